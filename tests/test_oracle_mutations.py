@@ -1,0 +1,103 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch each one.
+
+A pin set that still passes with a mistake planted is too weak to trust the
+oracle with; every mutation below must make at least one pin fail.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle import metadata as M
+from tests import test_oracle_pins as P
+
+CHECKS = [
+    ("bruteforce", lambda: P.check_bruteforce()),
+    ("bruteforce_window", lambda: P.check_bruteforce(window=3)),
+    ("sdpa", lambda: P.check_sdpa()),
+    ("sdpa_window", lambda: P.check_sdpa(window=5)),
+    ("single_key", P.check_single_key),
+    ("uniform", P.check_uniform_scores),
+    ("merge", P.check_merge_closed_form),
+]
+
+
+def _all_pins_pass():
+    for _, fn in CHECKS:
+        try:
+            if not fn():
+                return False
+        except Exception:
+            return False
+    return True
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert _all_pins_pass()
+
+
+MUTATIONS = {
+    # GQA: interleaved instead of contiguous head groups
+    "gqa_interleaved": ("kv_head_of", lambda h, group: h % 2),
+    # causal alignment off by one in either direction
+    "causal_plus_one": ("query_position", lambda L, n, t: L - n + t + 1),
+    "causal_minus_one": ("query_position", lambda L, n, t: max(0, L - n + t - 1)),
+    # top-left instead of bottom-right aligned causal mask
+    "causal_top_left": ("query_position", lambda L, n, t: t),
+    # window keeps w keys instead of w + 1
+    "window_w_keys": ("visible_range", lambda p, w: ((0 if w < 0 else max(0, p - w + 1)), p)),
+    # ignore last_page_len: treat the last page as full
+    "full_last_page": ("kv_len_of", lambda n, last, ps: n * ps),
+    # last page length off by one
+    "last_page_off_by_one": ("kv_len_of", lambda n, last, ps: 0 if n == 0 else (n - 1) * ps + last - 1),
+    # gather by offset only within the first page
+    "gather_ignores_pages": ("gather_logical", lambda pool, pages, L, ps: pool[np.asarray(pages)[np.zeros(L, dtype=np.int64)], np.arange(L) % ps]),
+    # drop the softmax scale
+    "no_scale": ("attend", None),
+    # transposed operand: V rows taken from K
+    "v_from_k": ("attend", None),
+}
+
+
+def _mutated_attend(kind):
+    import math
+
+    def no_scale(q, K, V, lo, hi, scale):
+        s = K[lo:hi + 1] @ q
+        m = s.max()
+        e = np.exp(s - m)
+        return (e @ V[lo:hi + 1]) / e.sum(), m + math.log(e.sum())
+
+    def v_from_k(q, K, V, lo, hi, scale):
+        s = (K[lo:hi + 1] @ q) * scale
+        m = s.max()
+        e = np.exp(s - m)
+        return (e @ K[lo:hi + 1]) / e.sum(), m + math.log(e.sum())
+
+    return {"no_scale": no_scale, "v_from_k": v_from_k}[kind]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(monkeypatch, name):
+    attr, fn = MUTATIONS[name]
+    if fn is None:
+        fn = _mutated_attend(name)
+    monkeypatch.setattr(A, attr, fn)
+    assert not _all_pins_pass(), f"mutation {name} survived every pin"
+
+
+def test_merge_with_swapped_weights_is_caught(monkeypatch):
+    def bad(o1, s1, o2, s2):
+        m = np.maximum(s1, s2)
+        w1, w2 = np.exp(s2 - m), np.exp(s1 - m)
+        return (o1 * w1 + o2 * w2) / (w1 + w2), m + np.log(w1 + w2)
+
+    monkeypatch.setattr(A, "merge_states", bad)
+    assert not P.check_merge_closed_form()
+
+
+def test_csr_with_zero_remainder_is_caught(monkeypatch):
+    # a remainder of 0 written as 0 instead of a full page
+    monkeypatch.setattr(M, "last_page_len_for", lambda L, ps: L % ps)
+    with pytest.raises(AssertionError):
+        P.test_vllm_worked_example_slot_mapping_and_csr()
