@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV attention hot path on GB300.
+
+Headline step (workload "llama8b_decode": batch 64, 32 q / 8 kv heads, head_dim 128, bf16, KV
+lengths U[512, 4096], page size 16, pages randomly permuted in a pool 1.25x the need): one pass of
+the path for one batch = plan (host work + metadata copy) + KV write of the 64 new tokens + paged
+decode (+ split-KV merge).  Metric: KV-read GB/s = algorithmic K/V bytes the decode must read
+(every visible key row, K and V, every KV head) / step time.
+
+Also measured (same JSON line, "prefill" object): the prefix-cached extend workload (batch 8, new
+U[128, 2048], prefix U[0, 4096], page size 1) as TFLOP/s over the causally visible (query, key)
+pairs, when the prefill kernel is built.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1: launched by torch.distributed.run, one rank per GPU; every rank runs its own independent
+batch (weak scaling, no data-path collective); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_HBM_GBS = 6800.0
+DEFAULT_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return DEFAULT_HBM_GBS, DEFAULT_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def _src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_attention_slot_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, source_files):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_hash") != _src_hash(*source_files):
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.lines = []
+        self.proc = None
+        self.device_index = device_index
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits", "-lms", "200"]
+        uuid = None
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+        except Exception:
+            pass
+        if uuid:
+            cmd += ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle baseline (spawned process pool; one task = one request)
+# ------------------------------------------------------------------------------------------------
+_WORKER_BATCH = None
+
+
+def _oracle_worker_init(workload_n, seed_offset):
+    """Each worker regenerates the seeded batch once (untimed), so tasks carry only request ids."""
+    global _WORKER_BATCH
+    import numpy as np
+    import torch
+
+    import workloads as W
+
+    b = W.workload(workload_n, seed_offset=seed_offset)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    _WORKER_BATCH = (b, bits(b.q), bits(b.k_pool), bits(b.v_pool))
+
+
+def _oracle_request_task(i):
+    """Worker: the oracle, as it stands, on request i of the batch (its one query token)."""
+    import numpy as np
+
+    from oracle import attention as OA
+
+    b, qb, kb, vb = _WORKER_BATCH
+    o, _ = OA.paged_attention(qb, kb, vb, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.page_size,
+                              sm_scale=b.sm_scale if b.sm_scale > 0 else None, window_left=b.window_left,
+                              q_format="bf16_bits", kv_format="bf16_bits", rows=[int(b.qo_indptr[i])])
+    return float(np.nansum(o))
+
+
+class OraclePool:
+    def __init__(self, workload_n=2, seed_offset=0):
+        import multiprocessing as mp
+
+        self.cores = max(1, os.cpu_count() or 1)
+        env = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+        old = {k: os.environ.get(k) for k in env}
+        os.environ.update(env)
+        try:
+            self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_worker_init,
+                                                     initargs=(workload_n, seed_offset))
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, b, req_ids):
+        """Wall time of the oracle over these requests, one request per task."""
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_request_task, list(req_ids), chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def _kv_bytes(b, req_ids):
+    import numpy as np
+
+    L = b.kv_len[np.asarray(req_ids)]
+    if b.window_left >= 0:
+        L = np.minimum(L, b.window_left + 1)
+    elem = 1 if b.kv_dtype == "e4m3" else 2
+    return int(L.sum()) * b.num_kv_heads * b.head_dim * elem * 2
+
+
+def cpu_baseline(b, pool, target_s=12.0):
+    """The oracle, as it stands, on the host cores: whole batches repeated until ~target_s of work."""
+    ids = list(range(b.batch_size))
+    pool.run(b, ids[: min(4, len(ids))])  # warm the workers
+    reps, total_t = 0, 0.0
+    while total_t < target_s and reps < 50:
+        total_t += pool.run(b, ids)
+        reps += 1
+    gbs = _kv_bytes(b, ids) * reps / total_t / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+            "sample": f"{reps} x the full {b.batch_size}-request batch ({_kv_bytes(b, ids) / 1e6:.1f} MB of KV each), "
+                      f"one request per task on a spawn pool of {pool.cores} single-threaded processes, "
+                      f"fp64 numpy oracle as it stands, wall clock"}
+
+
+# ------------------------------------------------------------------------------------------------
+# the GPU arm
+# ------------------------------------------------------------------------------------------------
+def _device_state(b, device):
+    import torch
+
+    import paged_kv_attention_slot_gb300 as pk
+
+    st = {}
+    st["k_pool"] = b.k_pool.to(device)
+    st["v_pool"] = b.v_pool.to(device)
+    st["cache"] = pk.KVCache(st["k_pool"], st["v_pool"])
+    st["q"] = b.q.to(device)
+    st["k_new"] = b.k_new.to(device)
+    st["v_new"] = b.v_new.to(device)
+    st["slots"] = torch.from_numpy(b.slot_mapping).to(device)
+    st["out"] = torch.empty_like(st["q"])
+    return st
+
+
+def _plan_kw(b):
+    return dict(num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
+                page_size=b.page_size, mode=b.mode, window_left=b.window_left, sm_scale=b.sm_scale,
+                kv_dtype=b.kv_dtype)
+
+
+def run_steps(b, st, plan, steps, warmup, dist_on, record_run_events=True):
+    """Warm up, then time exactly `steps` steps on the device (CUDA events), inputs resident."""
+    import torch
+
+    import paged_kv_attention_slot_gb300 as pk
+
+    kw = _plan_kw(b)
+    stream = torch.cuda.current_stream()
+    run_ev = []
+
+    def step(i, timed):
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **kw)
+        pk.kv_store(st["k_new"], st["v_new"], st["slots"], st["cache"])
+        if timed and record_run_events:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            plan.run(st["q"], st["cache"], out=st["out"])
+            e1.record(stream)
+            run_ev.append((e0, e1))
+        else:
+            plan.run(st["q"], st["cache"], out=st["out"])
+
+    for i in range(warmup):
+        step(i, False)
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(i, True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist_on:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    run_ms = [a.elapsed_time(c) for a, c in run_ev]
+    return total_ms, run_ms
+
+
+def run_e2e(b, st, plan, steps, warmup):
+    """Same step through the public API from pinned HOST buffers: H2D of the step's inputs, D2H of O."""
+    import torch
+
+    import paged_kv_attention_slot_gb300 as pk
+
+    kw = _plan_kw(b)
+    hq = b.q.pin_memory()
+    hk = b.k_new.pin_memory()
+    hv = b.v_new.pin_memory()
+    hs = torch.from_numpy(b.slot_mapping).pin_memory()
+    hout = torch.empty_like(b.q).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st["q"].copy_(hq, non_blocking=True)
+        st["k_new"].copy_(hk, non_blocking=True)
+        st["v_new"].copy_(hv, non_blocking=True)
+        st["slots"].copy_(hs, non_blocking=True)
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **kw)
+        pk.kv_store(st["k_new"], st["v_new"], st["slots"], st["cache"])
+        plan.run(st["q"], st["cache"], out=st["out"])
+        hout.copy_(st["out"], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t0
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs))
+    h2d += sum(a.nbytes for a in (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len))
+    d2h = hout.numel() * hout.element_size()
+    return dt, h2d, d2h
+
+
+def prefill_measure(device, steps, warmup, peak_tflops):
+    """Prefix-cached extend (page size 1): plan + KV write + prefill per step, TFLOP/s."""
+    import numpy as np
+    import torch
+
+    import paged_kv_attention_slot_gb300 as pk
+    import workloads as W
+
+    b = W.workload(3)
+    st = _device_state(b, device)
+    plan = pk.Plan()
+    try:
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **_plan_kw(b))
+    except pk.PkvError as e:
+        return {"unavailable": e.message}
+    # algorithmic FLOPs: 4 * D * Hq * sum over requests of the causally visible (query, key) pairs
+    n = b.q_len.astype(np.float64)
+    p = (b.kv_len - b.q_len).astype(np.float64)
+    pairs = float(np.sum(n * p + n * (n + 1) / 2))
+    flops = 4.0 * b.head_dim * b.num_qo_heads * pairs
+    total_ms, run_ms = run_steps(b, st, plan, steps, warmup, False)
+    run_avg = statistics.mean(run_ms)
+    achieved = flops / (run_avg * 1e-3) / 1e12
+    return {
+        "workload": "prefix_extend: batch 8, new U[128,2048], prefix U[0,4096], page 1, 32q/8kv, D 128, bf16",
+        "metric": "prefill TFLOP/s (causally visible pairs)",
+        "value": round(flops * steps / (total_ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "ms_per_step": round(total_ms / steps, 4),
+        "flops_per_step": flops,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tflops, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tflops, 4),
+                     "traffic": _traffic("prefill", ["prefill.cu", "ptx.cuh"])},
+        "run_ms_mean": round(run_avg, 4),
+        "gpu_launches_per_step": 2,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+
+    import paged_kv_attention_slot_gb300 as pk
+    import workloads as W
+
+    # the oracle pool is spawned before the first GPU call
+    pool = OraclePool(2, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    dist_on = world > 1
+    if dist_on:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    pk._lib.lib()
+    hbm, tf_burst, tf_sust, peak_src = _peaks()
+
+    b = W.workload(2, seed_offset=rank)
+    st = _device_state(b, device)
+    plan = pk.Plan()
+    plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **_plan_kw(b))
+    info = plan.info()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    total_ms, run_ms = run_steps(b, st, plan, args.steps, args.warmup, dist_on)
+    clk = clocks.stop()
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if dist_on:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    max_ms = float(t.item())
+    kv_bytes = b.kv_bytes_read()
+    value = kv_bytes * args.steps * world / (max_ms * 1e-3) / 1e9
+
+    e2e_dt, h2d, d2h = run_e2e(b, st, plan, max(3, args.steps // 2), 3)
+    e2e_val = kv_bytes * max(3, args.steps // 2) / e2e_dt / 1e9
+    err = pk.device_error()
+
+    run_avg = statistics.mean(run_ms)
+    achieved = kv_bytes / (run_avg * 1e-3) / 1e9
+    launches_per_step = 2 + (1 if info["num_merge"] > 0 else 0)
+
+    prefill = None
+    if not args.no_prefill and rank == 0:
+        prefill = prefill_measure(device, max(5, args.steps // 2), 3, tf_burst)
+
+    cpu = None
+    if pool is not None:
+        cpu = cpu_baseline(b, pool)
+        pool.close()
+
+    if rank == 0:
+        line = {
+            "metric": "paged decode KV-read GB/s (% of HBM) and prefill TFLOP/s (% of bf16 peak)",
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(max_ms / args.steps, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 values, random page permutation)",
+            "config": {
+                "workload": "llama8b_decode: batch 64, 32 q / 8 kv heads, head_dim 128, bf16 KV, "
+                            "KV length U[512,4096], page 16, pool 1.25x, step = plan + kv_store + decode",
+                "batch": b.batch_size, "kv_tokens": int(b.kv_len.sum()), "kv_bytes_per_step": kv_bytes,
+                "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB), no flush" % (
+                    2 * st["k_pool"].numel() * 2 / 1e6),
+                "parallelism": f"dp{world} (independent batches per GPU)",
+                "plan": {"ctas": info["num_work"], "merge_units": info["num_merge"], "kv_chunk": info["kv_chunk"]},
+            },
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                         "kernel": "decode_run (decode + split-KV merge kernels)",
+                         "traffic": _traffic("decode", ["decode.cu", "ptx.cuh"])},
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+            "prefill": prefill,
+            "device_error": err,
+        }
+        print(json.dumps(line))
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+def reference_arm(args, world, rank):
+    """The oracle, as it stands, on the host cores; same workload, metric and unit as the GPU arm."""
+    if rank != 0:
+        return
+    import workloads as W
+
+    pool = OraclePool(2, 0)
+    b = W.workload(2)
+    ids = list(range(b.batch_size))
+    per_step = ids[:8]  # bounded sample per step: 8 of the 64 requests
+    for _ in range(args.warmup):
+        pool.run(b, per_step[:2])
+    total = 0.0
+    for _ in range(args.steps):
+        total += pool.run(b, per_step)
+    pool.close()
+    kv = _kv_bytes(b, per_step)
+    value = kv * args.steps / total / 1e9
+    sample = (f"each step: 8 of the 64 requests of the llama8b_decode batch ({kv / 1e6:.1f} MB of KV), fp64 numpy "
+              f"oracle, one request per task on a spawn pool of {pool.cores} single-threaded processes")
+    line = {
+        "impl": "reference",
+        "metric": "paged decode KV-read GB/s (% of HBM) and prefill TFLOP/s (% of bf16 peak)",
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 values, random page permutation)",
+        "config": {"workload": "llama8b_decode: batch 64, 32 q / 8 kv heads, head_dim 128, bf16 KV, "
+                               "KV length U[512,4096], page 16, pool 1.25x"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": pool.cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

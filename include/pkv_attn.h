@@ -1,0 +1,284 @@
+/*
+ * pkv_attn.h -- C ABI of a GB300 (sm_103a) library for batched attention over a paged KV cache.
+ *
+ * The calls follow the plan-once-per-batch / run-per-layer contract the pages describe:
+ *   - "vLLM 源码完全拆解（六）：Attention Backend", section «plan() 与 run() 分别做什么»: plan()
+ *     consumes the batch's variable-length structure once; run() receives only this layer's Q and
+ *     the KV cache view and reuses the plan.
+ *   - "FlashInfer and the attention-backend abstraction", section «What plan() actually computes»:
+ *     the plan takes shape and policy only (no data tensors), picks the kernel specialisation,
+ *     assigns work tiles to CTAs and sizes the split-K temporaries inside a caller-owned workspace.
+ *   - "手写 mini-sglang 阶段四 · GPU 注意力后端", section «FlashInfer：plan 与 run»: plan() computes
+ *     the work partition on the CPU and copies it to the GPU asynchronously; the pinned staging
+ *     buffer it reuses must not be rewritten before the previous copy has finished.
+ *
+ * Conventions shared by every call:
+ *   - Pointers named "host" are CPU memory; every other data pointer is device memory on the
+ *     current CUDA device.  The library allocates NO device memory: every device buffer
+ *     (caches, Q, O, LSE, the plan workspace) belongs to the caller.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All device
+ *     work of a call is enqueued on that stream; no call synchronises the device except
+ *     pkv_attn_plan (which waits for ITS OWN previous host-to-device copy, see below) and
+ *     pkv_device_error.
+ *   - Every call returns a pkv_status.  On a non-OK status nothing was enqueued, and
+ *     pkv_last_error() returns a message (thread-local) naming the violated condition.  Nothing
+ *     ever falls back silently to another implementation ("vLLM 源码完全拆解（六）：Attention
+ *     Backend", section «自动选择与手工指定语义不同»: an explicit choice that cannot be honoured
+ *     fails loudly).
+ *   - Element counts and strides are in ELEMENTS, not bytes.
+ */
+#ifndef PKV_ATTN_H_
+#define PKV_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------------------------------------- */
+/* status codes and element types                                                                 */
+/* ---------------------------------------------------------------------------------------------- */
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,        /* an argument violates the documented contract                     */
+  PKV_EUNSUPPORTED = -2,  /* a valid request this build does not implement (never a fallback) */
+  PKV_EWORKSPACE = -3,    /* the workspace is too small (or missing) for this plan            */
+  PKV_ECUDA = -4,         /* a CUDA runtime/driver call or kernel launch failed               */
+  PKV_EDEVICE = -5        /* a kernel recorded an error in the device error word              */
+} pkv_status;
+
+typedef enum {
+  PKV_BF16 = 0,     /* bfloat16                                                            */
+  PKV_FP8_E4M3 = 1  /* OCP FP8 E4M3 ("fn"): code bytes; real value = decode(code) * scale     */
+} pkv_dtype;
+
+typedef enum {
+  PKV_MODE_DECODE = 0,  /* one new token per request (qo_indptr[i+1] - qo_indptr[i] in {0, 1}) */
+  PKV_MODE_PREFILL = 1  /* any number of new tokens per request (prefill / prefix-cached extend) */
+} pkv_mode;
+
+/* Device error codes a kernel may record (read with pkv_device_error). */
+enum {
+  PKV_DEVERR_NONE = 0,
+  PKV_DEVERR_SLOT_RANGE = 1,   /* kv_store: slot_mapping entry >= num_pages * page_size           */
+  PKV_DEVERR_PAGE_RANGE = 2,   /* attention: a page id outside [0, num_pages)                     */
+  PKV_DEVERR_TIMEOUT = 3       /* a bounded wait inside a kernel ran out; the kernel returned     */
+};
+
+/* ---------------------------------------------------------------------------------------------- */
+/* one layer's KV pool                                                                            */
+/* ---------------------------------------------------------------------------------------------- */
+/*
+ * Layout: K and V are separate pools, each logically [num_pages, page_size, num_kv_heads, head_dim]
+ * ("NHD"), with the innermost (head_dim) dimension contiguous and arbitrary strides for the other
+ * three ("vLLM 源码完全拆解（六）：Attention Backend", section «KV Cache 视图必须匹配 Kernel ABI»: the
+ * backend adapts strides and never copies the KV; "手写 mini-sglang 阶段四 · GPU 注意力后端": k_cache /
+ * v_cache of shape [pages, page_size, H, D]).  Element (p, t, h, d) of K is at
+ *   k + p * stride_page + t * stride_token + h * stride_head + d.
+ * Token slot s lives at page s / page_size, offset s % page_size.
+ * Requirements: k and v 16-byte aligned; stride_page, stride_token, stride_head multiples of
+ * 16 / element_size; head_dim in {64, 128}.  The prefill path further requires the slots to form
+ * one uniform row space (stride_page == page_size * stride_token) and head_dim == 128.
+ * FP8 pools hold E4M3 codes; k_scale / v_scale (> 0, finite) define real = code * scale on both the
+ * write and the read side ("SGLang 源码完全拆解(八)：Attention Backend", section «层与后端的边界»).
+ */
+typedef struct pkv_cache {
+  void* k;
+  void* v;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t dtype; /* pkv_dtype */
+  int64_t stride_page;
+  int64_t stride_token;
+  int64_t stride_head;
+  float k_scale; /* FP8 only */
+  float v_scale; /* FP8 only */
+} pkv_cache;
+
+/* ---------------------------------------------------------------------------------------------- */
+/* the KV write                                                                                   */
+/* ---------------------------------------------------------------------------------------------- */
+/*
+ * pkv_kv_store: write this step's K/V rows into the pool through slot_mapping, BEFORE attention
+ * reads the cache on the same stream ("vLLM 源码完全拆解（六）：Attention Backend", sections
+ * «Runner 先构造公共事实» (slot = physical_page * page_size + offset_in_page) and «为什么 KV 写入在
+ * Attention 之前»; "手写 mini-sglang 阶段四 · GPU 注意力后端": store_kv(k, v, out_loc, layer)).
+ *
+ *   k, v          device, bf16, [num_tokens, cache->num_kv_heads, cache->head_dim], contiguous.
+ *   slot_mapping  device, int64, [num_tokens].  A negative entry marks a padding token: nothing is
+ *                 written for it.  An entry >= num_pages * page_size is skipped and recorded as
+ *                 PKV_DEVERR_SLOT_RANGE in the device error word.
+ *   cache         host pointer to the pool description (read during the call only).
+ * BF16 pools receive a bit-exact copy.  FP8 pools receive code = E4M3_RNE_satfinite(float(x) *
+ * inv_scale) with inv_scale = 1.0f / scale computed once in float32 on the host.
+ * Two tokens mapped to the same slot in one call race; the caller must not do that.
+ * num_tokens == 0 is a no-op.
+ */
+int pkv_kv_store(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                 const pkv_cache* cache, void* stream);
+
+/* ---------------------------------------------------------------------------------------------- */
+/* the plan                                                                                       */
+/* ---------------------------------------------------------------------------------------------- */
+/*
+ * The batch is described by the CSR page table of "SGLang 源码完全拆解(八)：Attention Backend",
+ * section «统一元数据的编译», and "vLLM 源码完全拆解（六）：Attention Backend", section «从二维 Block
+ * Table 到 CSR 页表»:
+ *   qo_indptr      host int32 [batch_size + 1]: new-token row ranges in Q / O; qo_indptr[0] == 0,
+ *                  non-decreasing.  n_i = qo_indptr[i+1] - qo_indptr[i].
+ *   kv_indptr      host int32 [batch_size + 1]: page ranges in kv_indices; kv_indptr[0] == 0,
+ *                  non-decreasing.
+ *   kv_indices     host int32 [kv_indptr[batch_size]]: physical page ids, each request's pages in
+ *                  logical order; every id >= 0 (checked against the pool size at run time).
+ *   last_page_len  host int32 [batch_size]: valid tokens on each request's last page, in
+ *                  [1, page_size] (a full last page is page_size, never 0); ignored for a request
+ *                  with no pages.
+ * The KV length of request i is L_i = (pages_i - 1) * page_size + last_page_len[i] (0 without
+ * pages) and INCLUDES this step's new tokens (already written by pkv_kv_store).  New token t of
+ * request i sits at absolute position P = L_i - n_i + t and attends to keys j <= P (causal,
+ * bottom-right aligned: "手写 mini-sglang 阶段四 · GPU 注意力后端", section «在 CPU 上验证»), and with
+ * window_left = w >= 0 only to keys j >= P - w ("SGLang 源码完全拆解(八)：Attention Backend",
+ * section «mask 从哪里来»).  Query head h reads KV head h / (num_qo_heads / num_kv_heads).
+ * Checked: L_i >= n_i; L_i == 0 only if n_i == 0 (invariants 3-6 of "vLLM 源码完全拆解（六）：
+ * Attention Backend", section «九条必须成立的不变量»).
+ */
+typedef struct pkv_plan_args {
+  int32_t batch_size;
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* last_page_len;
+  int32_t num_qo_heads;  /* multiple of num_kv_heads                                         */
+  int32_t num_kv_heads;
+  int32_t head_dim;      /* 64 or 128 (decode); 128 (prefill)                                */
+  int32_t page_size;     /* >= 1                                                             */
+  int32_t mode;          /* pkv_mode                                                         */
+  int32_t causal;        /* must be 1                                                        */
+  int32_t window_left;   /* -1: no window; w >= 0 keeps keys P - w .. P                       */
+  float sm_scale;        /* <= 0 selects 1 / sqrt(head_dim)                                  */
+  int32_t q_dtype;       /* PKV_BF16                                                         */
+  int32_t kv_dtype;      /* PKV_BF16 or PKV_FP8_E4M3 (FP8 KV: decode mode only)               */
+  int32_t max_splits;    /* split-KV chunks per (request, KV head): 0 = planner's choice,    */
+                         /* 1 = never split, k > 1 = at most k                               */
+  int32_t num_sms;       /* SMs to plan for; 0 = query the current device                    */
+} pkv_plan_args;
+
+typedef struct pkv_plan pkv_plan; /* opaque; owns host memory (including pinned staging) only */
+
+/* Create an empty plan object.  It owns a pinned host staging buffer that grows on demand and is
+ * reused by every pkv_attn_plan call on this object. */
+int pkv_plan_create(pkv_plan** out);
+
+/* Destroy a plan: waits for its last host-to-device copy, then frees its host memory.  The
+ * caller's workspace is untouched.  NULL is a no-op. */
+void pkv_plan_destroy(pkv_plan* plan);
+
+/* Exact workspace bytes pkv_attn_plan needs for these arguments (validates them first). */
+int pkv_plan_workspace_size(const pkv_plan_args* args, size_t* bytes);
+
+/*
+ * pkv_attn_plan: validate the batch, copy its host arrays, build the CTA work list (split-KV
+ * chunks for decode, query tiles for prefill, longest first), lay out the workspace and enqueue ONE
+ * host-to-device copy of the metadata from the plan's pinned staging buffer into `workspace` on
+ * `stream`.  Before rewriting the staging buffer it waits for this plan object's previous copy.
+ * The host arrays may be reused by the caller as soon as the call returns.
+ *   workspace       device, 256-byte aligned, >= pkv_plan_workspace_size() bytes; it must stay
+ *                   allocated and unmodified until the last run that uses this plan has finished.
+ *                   workspace == NULL builds a HOST-ONLY plan (for inspection: pkv_plan_info,
+ *                   pkv_plan_work_items); running it returns PKV_EINVAL.
+ * A re-plan invalidates the previous plan held by the same object.
+ */
+int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/* ---------------------------------------------------------------------------------------------- */
+/* the runs (once per layer)                                                                      */
+/* ---------------------------------------------------------------------------------------------- */
+/*
+ * pkv_attn_decode_run / pkv_attn_prefill_run: attention for every new token of the planned batch,
+ * reading K/V through the plan's page table from `cache`.
+ *   q    device, bf16, [total_tokens, num_qo_heads, head_dim], contiguous (total_tokens =
+ *        qo_indptr[batch_size] of the plan).
+ *   o    device, bf16, same shape as q: o[row, h, :] = sum_j softmax_j(scale * q.k_j) v_j.
+ *   lse  device float32 [total_tokens, num_qo_heads] or NULL: natural-log log-sum-exp of the scaled
+ *        scores of each row (the statistic "SGLang 源码完全拆解(八)：Attention Backend", section
+ *        «extend 的两种形态», merges states with).
+ * The cache geometry (heads, head_dim, dtype) must match the plan, and the plan's largest page id
+ * must be < cache->num_pages (checked on the host, O(1)).  decode_run needs a PKV_MODE_DECODE plan,
+ * prefill_run a PKV_MODE_PREFILL plan.  Rows of requests with n_i == 0 do not exist; no other row
+ * of o is left unwritten.  The runs allocate nothing, read no host data of the batch and never
+ * synchronise; several runs (e.g. one per layer) may share one plan as long as the workspace is not
+ * used by two runs at the same time.
+ */
+int pkv_attn_decode_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                        void* stream);
+int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------------------------- */
+/* errors and inspection                                                                          */
+/* ---------------------------------------------------------------------------------------------- */
+/* Message of the last non-OK status returned on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* Synchronise `stream`, read the device error word of the current device into *code (a
+ * PKV_DEVERR_* value; the first error recorded wins) and clear it when reset != 0.  Returns
+ * PKV_EDEVICE when *code != 0. */
+int pkv_device_error(int32_t* code, int32_t reset, void* stream);
+
+typedef struct pkv_plan_info {
+  int32_t mode;
+  int32_t batch_size;
+  int64_t total_tokens;   /* qo_indptr[batch_size]                                       */
+  int64_t num_work;       /* CTAs of the main kernel                                      */
+  int64_t num_merge;      /* (request, KV head, head group) units that need a split merge */
+  int64_t num_partials;   /* partial (o, lse) slots in the workspace                      */
+  int64_t kv_chunk;       /* split-KV chunk length in tokens (decode)                      */
+  int64_t workspace_bytes;
+  int64_t max_page_id;    /* -1 if the batch has no pages                                  */
+  int64_t kv_tokens;      /* sum over requests of the keys the plan reads (per KV head)     */
+} pkv_plan_info;
+
+int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info);
+
+/* Copy the plan's work list to host memory: 8 int32 per CTA, in launch order:
+ *   {request, kv_head, head_group, kv_begin, kv_end, q_row, out_slot, q_rows}
+ * (out_slot = partial slot or -1 when the CTA writes the final output).  `capacity` is in int32. */
+int pkv_plan_work_items(const pkv_plan* plan, int32_t* out, int64_t capacity);
+
+/* ---------------------------------------------------------------------------------------------- */
+/* host helpers for building the plan inputs (no GPU needed)                                       */
+/* ---------------------------------------------------------------------------------------------- */
+/*
+ * 2-D block table -> CSR page table ("vLLM 源码完全拆解（六）：Attention Backend", section «从二维 Block
+ * Table 到 CSR 页表»; "FlashInfer and the attention-backend abstraction", section «What plan()
+ * actually computes»: a running sum of page counts, a gather of each row's valid prefix, a modulo).
+ *   block_table    host int32 [batch_size, max_pages] row-major (entries past a row's valid pages
+ *                  are ignored).
+ *   seq_lens       host int32 [batch_size], >= 0, ceil(seq_len / page_size) <= max_pages.
+ *   kv_indptr      host int32 [batch_size + 1] (out); kv_indices host int32 [capacity] (out);
+ *   last_page_len  host int32 [batch_size] (out; 0 for a request of length 0).
+ */
+int pkv_block_table_to_csr(const int32_t* block_table, int32_t batch_size, int32_t max_pages,
+                           const int32_t* seq_lens, int32_t page_size, int32_t* kv_indptr,
+                           int32_t* kv_indices, int64_t capacity, int32_t* last_page_len);
+
+/*
+ * Token-granular table -> page table: page_table[i, k] = token_table[i, k * page_size] / page_size
+ * for k < ceil(max(seq_lens) / page_size) ("手写 mini-sglang 阶段四 · GPU 注意力后端", section
+ * «FlashAttention：页号表»).  token_table host int32 [batch_size, table_width]; page_table host
+ * int32 [batch_size, ceil(max_len / page_size)] (out).
+ */
+int pkv_token_table_to_page_table(const int32_t* token_table, int32_t batch_size, int32_t table_width,
+                                  const int32_t* seq_lens, int32_t page_size, int32_t* page_table,
+                                  int64_t capacity);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* PKV_ATTN_H_ */

@@ -1,0 +1,236 @@
+"""Batched attention over a paged KV cache on GB300 (sm_103a): Python binding of libpkv_attn.so.
+
+The binding only marshals arguments; every step of the path (the KV write, the plan's device
+copy, decode, split-KV merge, prefill) runs in the library's CUDA kernels.  PyTorch supplies
+device memory and the current stream.
+
+Typical use (plan once per batch, run once per layer):
+
+    cache = KVCache(k_pool, v_pool)                     # [pages, page_size, kv_heads, head_dim]
+    kv_store(k_new, v_new, slot_mapping, cache)         # write this step's tokens first
+    plan = Plan()
+    plan.plan(qo_indptr, kv_indptr, kv_indices, last_page_len,
+              num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16, mode="decode")
+    out, lse = plan.run(q, cache, return_lse=True)
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import PkvError, check, lib
+
+__all__ = [
+    "KVCache", "Plan", "PkvError", "kv_store", "device_error", "block_table_to_csr",
+    "token_table_to_page_table", "library_path",
+]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+class KVCache:
+    """One layer's K and V pools, [num_pages, page_size, num_kv_heads, head_dim].
+
+    bf16 pools are torch.bfloat16 tensors; FP8 pools are torch.uint8 (or float8_e4m3fn) tensors of
+    E4M3 codes with k_scale / v_scale (real value = code * scale).  The last dimension must be
+    contiguous; other strides are passed through as they are.
+    """
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0):
+        if k.shape != v.shape or k.dim() != 4:
+            raise ValueError("k and v pools must both be [num_pages, page_size, num_kv_heads, head_dim]")
+        if k.stride() != v.stride():
+            raise ValueError("k and v pools must share strides")
+        if k.stride(3) != 1:
+            raise ValueError("head_dim must be the contiguous dimension")
+        if k.dtype == torch.bfloat16:
+            dtype = _lib.PKV_BF16
+        elif k.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+            dtype = _lib.PKV_FP8_E4M3
+        else:
+            raise ValueError(f"unsupported pool dtype {k.dtype}")
+        if v.dtype != k.dtype:
+            raise ValueError("k and v pools must have the same dtype")
+        self.k, self.v = k, v
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
+        self.dtype = dtype
+        self.struct = _lib.pkv_cache(
+            k.data_ptr(), v.data_ptr(), k.shape[0], k.shape[1], k.shape[2], k.shape[3], dtype,
+            k.stride(0), k.stride(1), k.stride(2), self.k_scale, self.v_scale)
+
+    @property
+    def num_pages(self):
+        return self.k.shape[0]
+
+    @property
+    def page_size(self):
+        return self.k.shape[1]
+
+    @property
+    def num_kv_heads(self):
+        return self.k.shape[2]
+
+    @property
+    def head_dim(self):
+        return self.k.shape[3]
+
+
+def kv_store(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, cache: KVCache, stream=None) -> None:
+    """Write k, v ([T, num_kv_heads, head_dim] bf16, contiguous) at slot_mapping ([T] int64, device)."""
+    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("k and v must be bf16")
+    if not (k.is_contiguous() and v.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("k, v and slot_mapping must be contiguous")
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    T = k.shape[0]
+    if v.shape != k.shape or slot_mapping.shape[0] != T or tuple(k.shape[1:]) != (cache.num_kv_heads, cache.head_dim):
+        raise ValueError("shape mismatch between k, v, slot_mapping and the cache")
+    check(lib().pkv_kv_store(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T, C.byref(cache.struct),
+                             _stream_ptr(stream)))
+
+
+def device_error(reset: bool = True, stream=None) -> int:
+    """Synchronise and read (and by default clear) the device error word; 0 means no error."""
+    code = C.c_int32(0)
+    st = lib().pkv_device_error(C.byref(code), 1 if reset else 0, _stream_ptr(stream))
+    if st not in (_lib.PKV_OK, _lib.PKV_EDEVICE):
+        check(st)
+    return int(code.value)
+
+
+class Plan:
+    """A reusable plan object: plan() once per batch, run() once per layer."""
+
+    def __init__(self):
+        h = C.c_void_p()
+        check(lib().pkv_plan_create(C.byref(h)))
+        self._h = h
+        self.workspace = None
+        self.mode = None
+        self._keep = None
+
+    def __del__(self):
+        try:
+            if getattr(self, "_h", None) is not None and self._h.value:
+                lib().pkv_plan_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+    @staticmethod
+    def _args(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads, head_dim, page_size,
+              mode, window_left, sm_scale, kv_dtype, max_splits, num_sms):
+        arrs = [_i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)]
+        B = len(arrs[3])
+        m = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL}[mode]
+        kd = {"bf16": _lib.PKV_BF16, "e4m3": _lib.PKV_FP8_E4M3, "fp8": _lib.PKV_FP8_E4M3}[kv_dtype]
+        a = _lib.pkv_plan_args(B, _ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(arrs[3]), num_qo_heads,
+                               num_kv_heads, head_dim, page_size, m, 1, window_left, float(sm_scale),
+                               _lib.PKV_BF16, kd, max_splits, num_sms)
+        return a, arrs
+
+    @staticmethod
+    def workspace_size(qo_indptr, kv_indptr, kv_indices, last_page_len, *, num_qo_heads, num_kv_heads, head_dim,
+                       page_size, mode="decode", window_left=-1, sm_scale=0.0, kv_dtype="bf16", max_splits=0,
+                       num_sms=0) -> int:
+        a, keep = Plan._args(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads,
+                             head_dim, page_size, mode, window_left, sm_scale, kv_dtype, max_splits, num_sms)
+        n = C.c_size_t(0)
+        check(lib().pkv_plan_workspace_size(C.byref(a), C.byref(n)))
+        return int(n.value)
+
+    def plan(self, qo_indptr, kv_indptr, kv_indices, last_page_len, *, num_qo_heads, num_kv_heads, head_dim,
+             page_size, mode="decode", window_left=-1, sm_scale=0.0, kv_dtype="bf16", max_splits=0, num_sms=0,
+             workspace: torch.Tensor | None = None, host_only: bool = False, stream=None) -> "Plan":
+        """Plan a batch.  Host int arrays in; the binding keeps a device workspace (grown on demand)."""
+        a, keep = self._args(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads, head_dim,
+                             page_size, mode, window_left, sm_scale, kv_dtype, max_splits, num_sms)
+        if host_only:
+            check(lib().pkv_attn_plan(self._h, C.byref(a), None, 0, None))
+        else:
+            n = C.c_size_t(0)
+            check(lib().pkv_plan_workspace_size(C.byref(a), C.byref(n)))
+            if workspace is not None:
+                self.workspace = workspace
+            elif self.workspace is None or self.workspace.numel() < n.value:
+                self.workspace = torch.empty(max(int(n.value), 1 << 16), dtype=torch.uint8, device="cuda")
+            check(lib().pkv_attn_plan(self._h, C.byref(a), self.workspace.data_ptr(), self.workspace.numel(),
+                                      _stream_ptr(stream)))
+        self.mode = mode
+        self.num_qo_heads = num_qo_heads
+        self.head_dim = head_dim
+        self.total_tokens = int(keep[0][-1]) if len(keep[0]) else 0
+        self._keep = keep
+        return self
+
+    def info(self) -> dict:
+        i = _lib.pkv_plan_info()
+        check(lib().pkv_plan_info_get(self._h, C.byref(i)))
+        return {f: getattr(i, f) for f, _ in i._fields_}
+
+    def work_items(self) -> np.ndarray:
+        n = self.info()["num_work"]
+        out = np.zeros(max(n, 1) * 8, dtype=np.int32)
+        check(lib().pkv_plan_work_items(self._h, _ptr(out), out.size))
+        return out[: n * 8].reshape(n, 8)
+
+    def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+            return_lse: bool = False, stream=None):
+        """Attention for every planned token row; q is [total_tokens, num_qo_heads, head_dim] bf16."""
+        if q.dtype != torch.bfloat16 or not q.is_contiguous():
+            raise ValueError("q must be a contiguous bf16 tensor")
+        if tuple(q.shape) != (self.total_tokens, self.num_qo_heads, self.head_dim):
+            raise ValueError(f"q must be [{self.total_tokens}, {self.num_qo_heads}, {self.head_dim}]")
+        if out is None:
+            out = torch.empty_like(q)
+        if (return_lse or lse is not None) and lse is None:
+            lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        fn = lib().pkv_attn_decode_run if self.mode == "decode" else lib().pkv_attn_prefill_run
+        check(fn(self._h, q.data_ptr(), C.byref(cache.struct), out.data_ptr(),
+                 lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
+        return (out, lse) if (return_lse or lse is not None) else out
+
+
+def block_table_to_csr(block_table, seq_lens, page_size: int):
+    """Host helper: 2-D block table -> (kv_indptr, kv_indices, last_page_len) int32 numpy arrays."""
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    B, W = bt.shape
+    indptr = np.zeros(B + 1, dtype=np.int32)
+    cap = max(1, B * W)
+    indices = np.zeros(cap, dtype=np.int32)
+    last = np.zeros(B, dtype=np.int32)
+    check(lib().pkv_block_table_to_csr(_ptr(bt), B, W, _ptr(sl), page_size, _ptr(indptr), _ptr(indices), cap,
+                                       _ptr(last)))
+    return indptr, indices[: indptr[-1]].copy(), last
+
+
+def token_table_to_page_table(token_table, seq_lens, page_size: int):
+    """Host helper: token-granular table -> page table (row[:max_len:page_size] // page_size)."""
+    tt = _i32(token_table)
+    sl = _i32(seq_lens)
+    B, W = tt.shape
+    cols = (int(sl.max()) + page_size - 1) // page_size if B else 0
+    out = np.zeros(max(1, B * cols), dtype=np.int32)
+    check(lib().pkv_token_table_to_page_table(_ptr(tt), B, W, _ptr(sl), page_size, _ptr(out), out.size))
+    return out[: B * cols].reshape(B, cols)

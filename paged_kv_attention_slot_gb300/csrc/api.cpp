@@ -1,0 +1,634 @@
+// C ABI and host planner for batched attention over a paged KV cache (GB300, sm_103a).
+//
+// The planner follows the plan/run split of "FlashInfer and the attention-backend abstraction",
+// section «What plan() actually computes» (shape and policy in, CTA work assignment and split-K
+// temporaries out) and "手写 mini-sglang 阶段四 · GPU 注意力后端", section «FlashInfer：plan 与 run»
+// (work partition computed on the CPU, copied to the GPU asynchronously through a reused pinned
+// buffer that is only rewritten after the previous copy has completed).
+//
+// Load balancing follows the idea of "SGLang 源码完全拆解(八)：Attention Backend", section «其他后端的
+// 元数据» (split long sequences into more KV chunks, spread ragged work evenly over CTAs using the
+// lengths): every (request, KV head, head group) is cut into chunks of one common length chosen
+// from the total work and the SM count, and the CTAs are launched longest first.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "pkv_internal.h"
+
+using pkv::MergeItem;
+using pkv::ReqInfo;
+using pkv::WorkItem;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+#define PKV_CUDA(expr, what)                                                        \
+  do {                                                                              \
+    cudaError_t _e = (expr);                                                        \
+    if (_e != cudaSuccess) return fail(PKV_ECUDA, std::string(what) + ": " + cudaGetErrorString(_e)); \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Decode kernel occupancy assumed by the split policy (it is launched with 2 CTAs per SM).
+constexpr int kDecodeCtasPerSm = 2;
+constexpr int kDecodeWaves = 4;          // target CTAs = SMs * CTAs/SM * waves
+constexpr int kDecodeMinChunk = 256;     // never split below this many keys
+constexpr int kDecodeChunkAlign = 64;    // 4 warps x 16 keys
+constexpr int kPrefillRows = 128;        // query rows (tokens x heads of one KV head) per CTA
+
+}  // namespace
+
+struct pkv_plan {
+  bool valid = false;
+  int32_t mode = 0, batch = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, window_left = -1, kv_dtype = 0, q_dtype = 0;
+  float sm_scale = 0.f;
+  int64_t total_tokens = 0, max_page_id = -1, kv_tokens = 0, kv_chunk = 0, num_partials = 0;
+  std::vector<WorkItem> work;
+  std::vector<MergeItem> merge;
+  std::vector<ReqInfo> req;
+  std::vector<int32_t> indices;
+  size_t off_work = 0, off_merge = 0, off_req = 0, off_idx = 0, off_plse = 0, off_po = 0;
+  size_t meta_bytes = 0, need_bytes = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  void* pinned = nullptr;
+  size_t pinned_bytes = 0;
+  cudaEvent_t copy_done = nullptr;
+  bool copy_pending = false;
+  int device = -1;
+};
+
+namespace {
+
+int query_num_sms(int32_t requested, int32_t* out) {
+  if (requested > 0) {
+    *out = requested;
+    return PKV_OK;
+  }
+  int dev = 0, n = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return fail(PKV_EINVAL, "num_sms == 0 needs a visible CUDA device; pass num_sms > 0 for a host-only plan");
+  }
+  *out = n;
+  return PKV_OK;
+}
+
+// Validate the arguments and build the work list into P (no device work).
+int build_plan(const pkv_plan_args* a, pkv_plan* P) {
+  if (!a) return fail(PKV_EINVAL, "args is NULL");
+  const int32_t B = a->batch_size;
+  if (B < 0) return fail(PKV_EINVAL, "batch_size < 0");
+  if (B > 0 && (!a->qo_indptr || !a->kv_indptr || !a->last_page_len))
+    return fail(PKV_EINVAL, "qo_indptr, kv_indptr and last_page_len must be non-NULL");
+  if (a->num_qo_heads <= 0 || a->num_kv_heads <= 0) return fail(PKV_EINVAL, "head counts must be positive");
+  if (a->num_qo_heads % a->num_kv_heads)
+    return fail(PKV_EINVAL, "num_qo_heads must be a multiple of num_kv_heads");
+  if (a->head_dim != 64 && a->head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (a->page_size < 1) return fail(PKV_EINVAL, "page_size must be >= 1");
+  if (a->mode != PKV_MODE_DECODE && a->mode != PKV_MODE_PREFILL) return fail(PKV_EINVAL, "unknown mode");
+  if (a->causal != 1) return fail(PKV_EUNSUPPORTED, "only causal (bottom-right aligned) attention is implemented");
+  if (a->window_left < -1) return fail(PKV_EINVAL, "window_left must be -1 or >= 0");
+  if (!(std::isfinite(a->sm_scale))) return fail(PKV_EINVAL, "sm_scale is not finite");
+  if (a->q_dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "q_dtype must be PKV_BF16");
+  if (a->kv_dtype != PKV_BF16 && a->kv_dtype != PKV_FP8_E4M3) return fail(PKV_EINVAL, "unknown kv_dtype");
+  if (a->kv_dtype == PKV_FP8_E4M3 && a->head_dim != 128)
+    return fail(PKV_EUNSUPPORTED, "FP8 KV needs head_dim 128");
+  if (a->max_splits < 0) return fail(PKV_EINVAL, "max_splits < 0");
+  const int32_t G = a->num_qo_heads / a->num_kv_heads;
+  if (a->mode == PKV_MODE_PREFILL) {
+    const char* why = nullptr;
+    if (!pkv::prefill_supported(&why)) return fail(PKV_EUNSUPPORTED, why ? why : "prefill kernel unavailable");
+    if (a->head_dim != 128) return fail(PKV_EUNSUPPORTED, "prefill needs head_dim 128");
+    if (a->kv_dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "prefill needs a bf16 KV cache");
+    if (G > kPrefillRows || kPrefillRows % G) return fail(PKV_EUNSUPPORTED, "prefill needs 128 % (Hq/Hkv) == 0");
+  }
+
+  if (B > 0) {
+    if (a->qo_indptr[0] != 0) return fail(PKV_EINVAL, "qo_indptr[0] must be 0");
+    if (a->kv_indptr[0] != 0) return fail(PKV_EINVAL, "kv_indptr[0] must be 0");
+  }
+  int64_t nnz = B > 0 ? a->kv_indptr[B] : 0;
+  if (nnz > 0 && !a->kv_indices) return fail(PKV_EINVAL, "kv_indices is NULL");
+
+  P->req.assign(B, ReqInfo{});
+  P->max_page_id = -1;
+  int64_t total_tokens = B > 0 ? a->qo_indptr[B] : 0;
+  for (int32_t i = 0; i < B; ++i) {
+    const int64_t n = (int64_t)a->qo_indptr[i + 1] - a->qo_indptr[i];
+    const int64_t np = (int64_t)a->kv_indptr[i + 1] - a->kv_indptr[i];
+    if (n < 0) return fail(PKV_EINVAL, "qo_indptr must be non-decreasing (request " + std::to_string(i) + ")");
+    if (np < 0) return fail(PKV_EINVAL, "kv_indptr must be non-decreasing (request " + std::to_string(i) + ")");
+    int64_t L = 0;
+    if (np > 0) {
+      const int32_t last = a->last_page_len[i];
+      if (last < 1 || last > a->page_size)
+        return fail(PKV_EINVAL, "last_page_len must be in [1, page_size] (request " + std::to_string(i) + ")");
+      L = (np - 1) * (int64_t)a->page_size + last;
+    }
+    if (L > INT32_MAX) return fail(PKV_EUNSUPPORTED, "KV length exceeds 2^31-1");
+    if (L < n)
+      return fail(PKV_EINVAL, "kv_len < q_len (request " + std::to_string(i) + "): seq_len - query_len must be the cached context");
+    if (a->mode == PKV_MODE_DECODE && n > 1)
+      return fail(PKV_EINVAL, "decode mode allows at most one new token per request (request " + std::to_string(i) + ")");
+    P->req[i] = ReqInfo{a->kv_indptr[i], (int32_t)L, a->qo_indptr[i], (int32_t)n};
+  }
+  P->indices.assign(a->kv_indices, a->kv_indices + nnz);
+  for (int64_t k = 0; k < nnz; ++k) {
+    if (P->indices[k] < 0) return fail(PKV_EINVAL, "kv_indices entries must be >= 0");
+    P->max_page_id = std::max<int64_t>(P->max_page_id, P->indices[k]);
+  }
+
+  int32_t sms = 0;
+  int st = query_num_sms(a->num_sms, &sms);
+  if (st != PKV_OK) return st;
+
+  P->mode = a->mode;
+  P->batch = B;
+  P->Hq = a->num_qo_heads;
+  P->Hkv = a->num_kv_heads;
+  P->D = a->head_dim;
+  P->ps = a->page_size;
+  P->window_left = a->window_left;
+  P->kv_dtype = a->kv_dtype;
+  P->q_dtype = a->q_dtype;
+  P->sm_scale = a->sm_scale > 0.f ? a->sm_scale : 1.0f / std::sqrt((float)a->head_dim);
+  P->total_tokens = total_tokens;
+  P->work.clear();
+  P->merge.clear();
+  P->num_partials = 0;
+  P->kv_tokens = 0;
+  P->kv_chunk = 0;
+
+  if (a->mode == PKV_MODE_DECODE) {
+    const int32_t groups = (G + pkv::kDecodeRows - 1) / pkv::kDecodeRows;
+    struct Unit { int32_t req, lo, hi; };
+    std::vector<Unit> units;
+    int64_t total = 0;
+    for (int32_t i = 0; i < B; ++i) {
+      if (P->req[i].q_len == 0) continue;
+      const int32_t L = P->req[i].kv_len;
+      const int32_t pos = L - 1;
+      const int32_t lo = a->window_left >= 0 ? std::max(0, pos - a->window_left) : 0;
+      units.push_back({i, lo, L});
+      total += (int64_t)(L - lo);
+    }
+    P->kv_tokens = total;
+    const int64_t work_total = total * a->num_kv_heads * groups;
+    int64_t chunk;
+    if (a->max_splits == 1) {
+      chunk = INT32_MAX;
+    } else {
+      const int64_t target = (int64_t)sms * kDecodeCtasPerSm * kDecodeWaves;
+      chunk = (work_total + target - 1) / std::max<int64_t>(1, target);
+      chunk = std::max<int64_t>(chunk, kDecodeMinChunk);
+      chunk = align_up(chunk, kDecodeChunkAlign);
+    }
+    P->kv_chunk = chunk;
+    int64_t slot = 0;
+    for (const Unit& u : units) {
+      const int64_t len = u.hi - u.lo;
+      int64_t ns = (len + chunk - 1) / chunk;
+      if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
+      int64_t c = (len + ns - 1) / ns;
+      c = align_up(c, 16);
+      ns = (len + c - 1) / c;
+      for (int32_t h = 0; h < a->num_kv_heads; ++h) {
+        for (int32_t g = 0; g < groups; ++g) {
+          const int32_t first = ns > 1 ? (int32_t)slot : -1;
+          for (int64_t s = 0; s < ns; ++s) {
+            WorkItem w;
+            w.req = u.req;
+            w.kv_head = h;
+            w.head_group = g;
+            w.kv_begin = (int32_t)(u.lo + s * c);
+            w.kv_end = (int32_t)std::min<int64_t>(u.hi, u.lo + (s + 1) * c);
+            w.q_row = P->req[u.req].q_begin;
+            w.out_slot = ns > 1 ? (int32_t)(slot + s) : -1;
+            w.q_rows = 1;
+            P->work.push_back(w);
+          }
+          if (ns > 1) {
+            MergeItem m{};
+            m.q_row = P->req[u.req].q_begin;
+            m.kv_head = h;
+            m.head_group = g;
+            m.first_slot = first;
+            m.num_splits = (int32_t)ns;
+            P->merge.push_back(m);
+            slot += ns;
+          }
+        }
+      }
+    }
+    P->num_partials = slot;
+  } else {
+    const int32_t tok_per_tile = kPrefillRows / G;
+    for (int32_t i = 0; i < B; ++i) {
+      const ReqInfo& r = P->req[i];
+      for (int32_t t0 = 0; t0 < r.q_len; t0 += tok_per_tile) {
+        const int32_t rows = std::min(tok_per_tile, r.q_len - t0);
+        const int32_t pos0 = r.kv_len - r.q_len + t0;
+        const int32_t last_pos = pos0 + rows - 1;
+        const int32_t lo = a->window_left >= 0 ? std::max(0, pos0 - a->window_left) : 0;
+        P->kv_tokens += (int64_t)(last_pos + 1 - lo);
+        for (int32_t h = 0; h < a->num_kv_heads; ++h) {
+          WorkItem w;
+          w.req = i;
+          w.kv_head = h;
+          w.head_group = 0;
+          w.kv_begin = lo;
+          w.kv_end = last_pos + 1;
+          w.q_row = r.q_begin + t0;
+          w.out_slot = -1;
+          w.q_rows = rows;
+          P->work.push_back(w);
+        }
+      }
+    }
+  }
+  // longest first: the block scheduler hands out CTAs roughly in launch order
+  std::stable_sort(P->work.begin(), P->work.end(), [](const WorkItem& x, const WorkItem& y) {
+    return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
+  });
+  if ((int64_t)P->work.size() > INT32_MAX) return fail(PKV_EUNSUPPORTED, "too many CTAs");
+
+  // workspace layout: [work][merge][req][kv_indices] | [partial lse][partial o]
+  size_t off = 0;
+  P->off_work = off;
+  off = align_up(off + P->work.size() * sizeof(WorkItem), 256);
+  P->off_merge = off;
+  off = align_up(off + P->merge.size() * sizeof(MergeItem), 256);
+  P->off_req = off;
+  off = align_up(off + P->req.size() * sizeof(ReqInfo), 256);
+  P->off_idx = off;
+  off = align_up(off + P->indices.size() * sizeof(int32_t), 256);
+  P->meta_bytes = off;
+  P->off_plse = off;
+  off = align_up(off + (size_t)P->num_partials * pkv::kDecodeRows * sizeof(float), 256);
+  P->off_po = off;
+  off = align_up(off + (size_t)P->num_partials * pkv::kDecodeRows * P->D * sizeof(float), 256);
+  P->need_bytes = std::max<size_t>(off, 256);
+  P->valid = true;
+  return PKV_OK;
+}
+
+int check_cache(const pkv_plan* P, const pkv_cache* c) {
+  if (!c) return fail(PKV_EINVAL, "cache is NULL");
+  if (!c->k || !c->v) return fail(PKV_EINVAL, "cache k/v pointers are NULL");
+  if (c->num_kv_heads != P->Hkv || c->head_dim != P->D || c->page_size != P->ps || c->dtype != P->kv_dtype)
+    return fail(PKV_EINVAL, "cache geometry (kv heads, head_dim, page_size, dtype) does not match the plan");
+  if (c->num_pages <= P->max_page_id)
+    return fail(PKV_EINVAL, "the plan references page " + std::to_string(P->max_page_id) + " but the pool has " +
+                                std::to_string(c->num_pages) + " pages");
+  const int64_t esz = c->dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const int64_t vec = 16 / esz;
+  if (((uintptr_t)c->k | (uintptr_t)c->v) & 15) return fail(PKV_EINVAL, "cache k/v must be 16-byte aligned");
+  if (c->stride_page % vec || c->stride_token % vec || c->stride_head % vec)
+    return fail(PKV_EINVAL, "cache strides must be multiples of 16 bytes");
+  if (c->stride_page <= 0 || c->stride_token <= 0 || c->stride_head <= 0)
+    return fail(PKV_EINVAL, "cache strides must be positive");
+  if (c->dtype == PKV_FP8_E4M3) {
+    if (!(c->k_scale > 0.f) || !(c->v_scale > 0.f) || !std::isfinite(c->k_scale) || !std::isfinite(c->v_scale))
+      return fail(PKV_EINVAL, "FP8 cache scales must be finite and > 0");
+  }
+  return PKV_OK;
+}
+
+pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c, void* o, float* lse) {
+  pkv::RunParams p{};
+  char* ws = (char*)P->ws;
+  p.work = (const WorkItem*)(ws + P->off_work);
+  p.merge = (const MergeItem*)(ws + P->off_merge);
+  p.req = (const ReqInfo*)(ws + P->off_req);
+  p.kv_indices = (const int32_t*)(ws + P->off_idx);
+  p.part_lse = (float*)(ws + P->off_plse);
+  p.part_o = (float*)(ws + P->off_po);
+  p.q = q;
+  p.o = o;
+  p.lse = lse;
+  const int64_t esz = c->dtype == PKV_FP8_E4M3 ? 1 : 2;
+  p.k_pool = (const char*)c->k;
+  p.v_pool = (const char*)c->v;
+  p.stride_page_b = c->stride_page * esz;
+  p.stride_token_b = c->stride_token * esz;
+  p.stride_head_b = c->stride_head * esz;
+  p.num_pages = c->num_pages;
+  p.page_size = P->ps;
+  p.num_qo_heads = P->Hq;
+  p.num_kv_heads = P->Hkv;
+  p.group = P->Hq / P->Hkv;
+  p.head_dim = P->D;
+  p.window_left = P->window_left;
+  const float log2e = 1.4426950408889634f;
+  p.scale_log2 = P->sm_scale * log2e * (c->dtype == PKV_FP8_E4M3 ? c->k_scale : 1.0f);
+  p.out_scale = c->dtype == PKV_FP8_E4M3 ? c->v_scale : 1.0f;
+  p.num_work = (int64_t)P->work.size();
+  p.num_merge = (int64_t)P->merge.size();
+  return p;
+}
+
+int check_run(const pkv_plan* P, int mode, const void* q, const pkv_cache* c, void* o) {
+  if (!P || !P->valid) return fail(PKV_EINVAL, "plan is NULL or has not been planned");
+  if (!P->ws) return fail(PKV_EINVAL, "the plan is host-only (planned without a workspace)");
+  if (P->mode != mode)
+    return fail(PKV_EINVAL, mode == PKV_MODE_DECODE ? "decode_run needs a PKV_MODE_DECODE plan"
+                                                    : "prefill_run needs a PKV_MODE_PREFILL plan");
+  int st = check_cache(P, c);
+  if (st != PKV_OK) return st;
+  if (P->total_tokens > 0 && (!q || !o)) return fail(PKV_EINVAL, "q and o must be non-NULL");
+  if (((uintptr_t)q | (uintptr_t)o) & 15) return fail(PKV_EINVAL, "q and o must be 16-byte aligned");
+  int dev = -1;
+  PKV_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev != P->device) return fail(PKV_EINVAL, "the current device is not the device the plan was made on");
+  return PKV_OK;
+}
+
+// ---- TMA tensor maps (driver entry point fetched at run time; no link against libcuda) ----
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_tiled() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+}  // namespace
+
+// ================================================================================================
+// C ABI
+// ================================================================================================
+extern "C" {
+
+const char* pkv_last_error(void) { return g_err.c_str(); }
+
+int pkv_plan_create(pkv_plan** out) {
+  if (!out) return fail(PKV_EINVAL, "out is NULL");
+  *out = new pkv_plan();
+  return PKV_OK;
+}
+
+void pkv_plan_destroy(pkv_plan* plan) {
+  if (!plan) return;
+  if (plan->copy_done) {
+    cudaEventSynchronize(plan->copy_done);
+    cudaEventDestroy(plan->copy_done);
+  }
+  if (plan->pinned) cudaFreeHost(plan->pinned);
+  cudaGetLastError();
+  delete plan;
+}
+
+int pkv_plan_workspace_size(const pkv_plan_args* args, size_t* bytes) {
+  if (!bytes) return fail(PKV_EINVAL, "bytes is NULL");
+  pkv_plan tmp;
+  int st = build_plan(args, &tmp);
+  if (st != PKV_OK) return st;
+  *bytes = tmp.need_bytes;
+  return PKV_OK;
+}
+
+int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan) return fail(PKV_EINVAL, "plan is NULL");
+  plan->valid = false;
+  // the pinned staging buffer may still be the source of the previous plan's copy
+  if (plan->copy_pending && plan->copy_done) {
+    PKV_CUDA(cudaEventSynchronize(plan->copy_done), "waiting for the previous plan copy");
+    plan->copy_pending = false;
+  }
+  int st = build_plan(args, plan);
+  if (st != PKV_OK) {
+    plan->valid = false;
+    return st;
+  }
+  plan->ws = nullptr;
+  plan->ws_bytes = 0;
+  if (!workspace) return PKV_OK;  // host-only plan
+  plan->valid = false;
+  if ((uintptr_t)workspace & 255) return fail(PKV_EINVAL, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan->need_bytes)
+    return fail(PKV_EWORKSPACE, "workspace has " + std::to_string(workspace_bytes) + " bytes, the plan needs " +
+                                    std::to_string(plan->need_bytes));
+  int dev = -1;
+  PKV_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (plan->pinned && plan->device != dev) {
+    // staging and event belong to another device: start over
+    if (plan->copy_done) cudaEventDestroy(plan->copy_done);
+    cudaFreeHost(plan->pinned);
+    plan->pinned = nullptr;
+    plan->pinned_bytes = 0;
+    plan->copy_done = nullptr;
+  }
+  plan->device = dev;
+  if (plan->pinned_bytes < plan->meta_bytes) {
+    if (plan->pinned) cudaFreeHost(plan->pinned);
+    plan->pinned = nullptr;
+    size_t want = std::max<size_t>(plan->meta_bytes, 64 << 10);
+    want = std::max<size_t>(want, plan->pinned_bytes * 2);
+    PKV_CUDA(cudaHostAlloc(&plan->pinned, want, cudaHostAllocDefault), "cudaHostAlloc (plan staging)");
+    plan->pinned_bytes = want;
+  }
+  if (!plan->copy_done) PKV_CUDA(cudaEventCreateWithFlags(&plan->copy_done, cudaEventDisableTiming), "cudaEventCreate");
+  char* h = (char*)plan->pinned;
+  std::memset(h, 0, plan->meta_bytes);
+  std::memcpy(h + plan->off_work, plan->work.data(), plan->work.size() * sizeof(WorkItem));
+  std::memcpy(h + plan->off_merge, plan->merge.data(), plan->merge.size() * sizeof(MergeItem));
+  std::memcpy(h + plan->off_req, plan->req.data(), plan->req.size() * sizeof(ReqInfo));
+  std::memcpy(h + plan->off_idx, plan->indices.data(), plan->indices.size() * sizeof(int32_t));
+  cudaStream_t s = (cudaStream_t)stream;
+  PKV_CUDA(cudaMemcpyAsync(workspace, h, plan->meta_bytes, cudaMemcpyHostToDevice, s), "plan metadata copy");
+  PKV_CUDA(cudaEventRecord(plan->copy_done, s), "cudaEventRecord");
+  plan->copy_pending = true;
+  plan->ws = workspace;
+  plan->ws_bytes = workspace_bytes;
+  plan->valid = true;
+  return PKV_OK;
+}
+
+int pkv_kv_store(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, const pkv_cache* cache,
+                 void* stream) {
+  if (num_tokens < 0) return fail(PKV_EINVAL, "num_tokens < 0");
+  if (!cache) return fail(PKV_EINVAL, "cache is NULL");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !cache->k || !cache->v) return fail(PKV_EINVAL, "NULL pointer argument");
+  if (cache->head_dim != 64 && cache->head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (cache->dtype != PKV_BF16 && cache->dtype != PKV_FP8_E4M3) return fail(PKV_EINVAL, "unknown cache dtype");
+  if (cache->num_kv_heads <= 0 || cache->page_size < 1 || cache->num_pages < 0)
+    return fail(PKV_EINVAL, "bad cache geometry");
+  const int64_t esz = cache->dtype == PKV_FP8_E4M3 ? 1 : 2;
+  const int64_t vec = cache->dtype == PKV_FP8_E4M3 ? 8 : 16;  // bytes each thread stores
+  if (((uintptr_t)k | (uintptr_t)v) & 15) return fail(PKV_EINVAL, "k and v must be 16-byte aligned");
+  if (((uintptr_t)cache->k | (uintptr_t)cache->v) & (vec - 1)) return fail(PKV_EINVAL, "cache k/v misaligned");
+  if ((cache->stride_page * esz) % vec || (cache->stride_token * esz) % vec || (cache->stride_head * esz) % vec)
+    return fail(PKV_EINVAL, "cache strides must be multiples of 16 bytes (bf16) or 8 bytes (fp8)");
+  float inv_k = 1.f, inv_v = 1.f;
+  if (cache->dtype == PKV_FP8_E4M3) {
+    if (!(cache->k_scale > 0.f) || !(cache->v_scale > 0.f) || !std::isfinite(cache->k_scale) ||
+        !std::isfinite(cache->v_scale))
+      return fail(PKV_EINVAL, "FP8 cache scales must be finite and > 0");
+    inv_k = 1.0f / cache->k_scale;
+    inv_v = 1.0f / cache->v_scale;
+  }
+  PKV_CUDA(pkv::launch_kv_store(k, v, slot_mapping, num_tokens, *cache, inv_k, inv_v, (cudaStream_t)stream),
+           "kv_store launch");
+  return PKV_OK;
+}
+
+int pkv_attn_decode_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                        void* stream) {
+  int st = check_run(plan, PKV_MODE_DECODE, q, cache, o);
+  if (st != PKV_OK) return st;
+  if (plan->work.empty()) return PKV_OK;
+  pkv::RunParams p = make_params(plan, q, cache, o, lse);
+  PKV_CUDA(pkv::launch_decode(p, cache->dtype, (cudaStream_t)stream), "decode launch");
+  if (!plan->merge.empty()) PKV_CUDA(pkv::launch_merge(p, (cudaStream_t)stream), "merge launch");
+  return PKV_OK;
+}
+
+int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                         void* stream) {
+  int st = check_run(plan, PKV_MODE_PREFILL, q, cache, o);
+  if (st != PKV_OK) return st;
+  if (plan->work.empty()) return PKV_OK;
+  if (cache->stride_page != (int64_t)cache->page_size * cache->stride_token)
+    return fail(PKV_EUNSUPPORTED, "prefill needs stride_page == page_size * stride_token (uniform slot rows)");
+  if (cache->stride_head != cache->head_dim)
+    return fail(PKV_EUNSUPPORTED, "prefill needs the heads of a token contiguous (stride_head == head_dim)");
+  auto encode = get_encode_tiled();
+  if (!encode) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+  alignas(64) CUtensorMap tq, tk, tv;
+  // Q: 3-D (head_dim, num_qo_heads, tokens), box (64, group, 128 / group), 128-byte swizzle
+  {
+    const int G = plan->Hq / plan->Hkv;
+    cuuint64_t dims[3] = {(cuuint64_t)plan->D, (cuuint64_t)plan->Hq, (cuuint64_t)plan->total_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)plan->D * 2, (cuuint64_t)plan->Hq * plan->D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = encode(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(Q) failed: " + std::to_string((int)r));
+  }
+  // K/V: 2-D (num_kv_heads * head_dim columns, num_pages * page_size slot rows), box (64, 1) for gather4
+  {
+    const int64_t rows = cache->num_pages * (int64_t)cache->page_size;
+    cuuint64_t dims[2] = {(cuuint64_t)cache->num_kv_heads * cache->head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cache->stride_token * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t es[2] = {1, 1};
+    if (rows > INT32_MAX) return fail(PKV_EUNSUPPORTED, "prefill needs num_pages * page_size < 2^31");
+    CUresult r = encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cache->k, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(K) failed: " + std::to_string((int)r));
+    r = encode(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cache->v, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(V) failed: " + std::to_string((int)r));
+  }
+  pkv::RunParams p = make_params(plan, q, cache, o, lse);
+  PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
+  return PKV_OK;
+}
+
+int pkv_device_error(int32_t* code, int32_t reset, void* stream) {
+  if (!code) return fail(PKV_EINVAL, "code is NULL");
+  PKV_CUDA(pkv::read_device_error(code, reset, (cudaStream_t)stream), "reading the device error word");
+  if (*code != 0) return fail(PKV_EDEVICE, "device error word = " + std::to_string(*code));
+  return PKV_OK;
+}
+
+int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info) {
+  if (!plan || !info) return fail(PKV_EINVAL, "NULL argument");
+  if (!plan->valid) return fail(PKV_EINVAL, "plan has not been planned");
+  info->mode = plan->mode;
+  info->batch_size = plan->batch;
+  info->total_tokens = plan->total_tokens;
+  info->num_work = (int64_t)plan->work.size();
+  info->num_merge = (int64_t)plan->merge.size();
+  info->num_partials = plan->num_partials;
+  info->kv_chunk = plan->kv_chunk;
+  info->workspace_bytes = (int64_t)plan->need_bytes;
+  info->max_page_id = plan->max_page_id;
+  info->kv_tokens = plan->kv_tokens;
+  return PKV_OK;
+}
+
+int pkv_plan_work_items(const pkv_plan* plan, int32_t* out, int64_t capacity) {
+  if (!plan || !out) return fail(PKV_EINVAL, "NULL argument");
+  if (!plan->valid) return fail(PKV_EINVAL, "plan has not been planned");
+  const int64_t need = (int64_t)plan->work.size() * 8;
+  if (capacity < need) return fail(PKV_EINVAL, "capacity too small: need " + std::to_string(need));
+  std::memcpy(out, plan->work.data(), need * sizeof(int32_t));
+  return PKV_OK;
+}
+
+int pkv_block_table_to_csr(const int32_t* block_table, int32_t batch_size, int32_t max_pages, const int32_t* seq_lens,
+                           int32_t page_size, int32_t* kv_indptr, int32_t* kv_indices, int64_t capacity,
+                           int32_t* last_page_len) {
+  if (batch_size < 0 || max_pages < 0 || page_size < 1) return fail(PKV_EINVAL, "bad sizes");
+  if (batch_size > 0 && (!block_table || !seq_lens || !kv_indptr || !last_page_len))
+    return fail(PKV_EINVAL, "NULL argument");
+  if (!kv_indptr) return fail(PKV_EINVAL, "kv_indptr is NULL");
+  kv_indptr[0] = 0;
+  int64_t at = 0;
+  for (int32_t i = 0; i < batch_size; ++i) {
+    const int64_t L = seq_lens[i];
+    if (L < 0) return fail(PKV_EINVAL, "seq_lens must be >= 0");
+    const int64_t np = (L + page_size - 1) / page_size;  // pages of this request
+    if (np > max_pages) return fail(PKV_EINVAL, "a row needs more pages than the block table is wide");
+    if (at + np > capacity) return fail(PKV_EINVAL, "kv_indices capacity too small");
+    if (at + np > INT32_MAX) return fail(PKV_EINVAL, "too many pages");
+    for (int64_t p = 0; p < np; ++p) kv_indices[at + p] = block_table[(int64_t)i * max_pages + p];
+    at += np;
+    kv_indptr[i + 1] = (int32_t)at;
+    last_page_len[i] = np ? (int32_t)(L - (np - 1) * page_size) : 0;  // a full last page is page_size
+  }
+  return PKV_OK;
+}
+
+int pkv_token_table_to_page_table(const int32_t* token_table, int32_t batch_size, int32_t table_width,
+                                  const int32_t* seq_lens, int32_t page_size, int32_t* page_table, int64_t capacity) {
+  if (batch_size < 0 || table_width < 0 || page_size < 1) return fail(PKV_EINVAL, "bad sizes");
+  if (batch_size == 0) return PKV_OK;
+  if (!token_table || !seq_lens || !page_table) return fail(PKV_EINVAL, "NULL argument");
+  int64_t max_len = 0;
+  for (int32_t i = 0; i < batch_size; ++i) max_len = std::max<int64_t>(max_len, seq_lens[i]);
+  if (max_len > table_width) return fail(PKV_EINVAL, "seq_len exceeds the token table width");
+  const int64_t cols = (max_len + page_size - 1) / page_size;
+  if (capacity < cols * batch_size) return fail(PKV_EINVAL, "page_table capacity too small");
+  for (int32_t i = 0; i < batch_size; ++i)
+    for (int64_t c = 0; c < cols; ++c)
+      page_table[i * cols + c] = token_table[(int64_t)i * table_width + c * page_size] / page_size;
+  return PKV_OK;
+}
+
+}  // extern "C"

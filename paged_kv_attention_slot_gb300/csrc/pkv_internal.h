@@ -1,0 +1,87 @@
+// Internal declarations shared by the host planner / C ABI (api.cpp) and the CUDA kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_attn.h"
+
+namespace pkv {
+
+// One CTA of a run kernel.  Same field order as the public pkv_plan_work_items() rows.
+struct WorkItem {
+  int32_t req;         // request index
+  int32_t kv_head;     // KV head
+  int32_t head_group;  // group of up to 16 query heads of this KV head (decode); 0 (prefill)
+  int32_t kv_begin;    // first key (logical position) this CTA reads
+  int32_t kv_end;      // one past the last key this CTA reads
+  int32_t q_row;       // first token row of Q / O
+  int32_t out_slot;    // decode: partial slot, or -1 = write the final output
+  int32_t q_rows;      // tokens of this request in this CTA's tile (decode: 1)
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
+
+// One (request, KV head, head group) whose split-KV partials must be merged.
+struct MergeItem {
+  int32_t q_row;
+  int32_t kv_head;
+  int32_t head_group;
+  int32_t first_slot;
+  int32_t num_splits;
+  int32_t pad0, pad1, pad2;
+};
+static_assert(sizeof(MergeItem) == 32, "MergeItem is 32 bytes");
+
+// Per-request facts the kernels need: page list start, KV length, first token row, token count.
+struct ReqInfo {
+  int32_t page_base;
+  int32_t kv_len;
+  int32_t q_begin;
+  int32_t q_len;
+};
+static_assert(sizeof(ReqInfo) == 16, "ReqInfo is 16 bytes");
+
+// Max query rows one decode CTA handles per KV head (one m16 MMA tile).
+constexpr int kDecodeRows = 16;
+
+// Everything a run kernel reads, passed by value.
+struct RunParams {
+  const WorkItem* work;
+  const MergeItem* merge;
+  const ReqInfo* req;
+  const int32_t* kv_indices;
+  float* part_o;    // [num_partials, 16, head_dim]
+  float* part_lse;  // [num_partials, 16] (log2 units)
+  const void* q;
+  void* o;
+  float* lse;  // nullable
+  const char* k_pool;
+  const char* v_pool;
+  int64_t stride_page_b;   // bytes
+  int64_t stride_token_b;  // bytes
+  int64_t stride_head_b;   // bytes
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t num_qo_heads;
+  int32_t num_kv_heads;
+  int32_t group;       // num_qo_heads / num_kv_heads
+  int32_t head_dim;
+  int32_t window_left;
+  float scale_log2;    // sm_scale * log2(e) (* k_scale for FP8 KV)
+  float out_scale;     // 1, or v_scale for FP8 KV
+  int64_t num_work;
+  int64_t num_merge;
+};
+
+// launchers (return cudaError_t of the launch)
+cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, int64_t T, const pkv_cache& c,
+                            float inv_k, float inv_v, cudaStream_t s);
+cudaError_t launch_decode(const RunParams& p, int kv_dtype, cudaStream_t s);
+cudaError_t launch_merge(const RunParams& p, cudaStream_t s);
+cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v,
+                           int64_t total_tokens, cudaStream_t s);
+int prefill_supported(const char** why);
+
+cudaError_t read_device_error(int32_t* code, int reset, cudaStream_t s);
+
+}  // namespace pkv

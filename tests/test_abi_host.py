@@ -1,0 +1,177 @@
+"""The C ABI on the host (no GPU): every declared symbol is exported, the host helpers reproduce the
+pages' worked examples, the planner rejects invalid batches loudly, and its split-KV / tile
+partition covers every key of every (request, KV head) exactly once."""
+
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_attention_slot_gb300 import build as B
+
+    B.build()
+    import paged_kv_attention_slot_gb300 as pk
+
+    pk._lib.lib()
+    return pk
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "pkv_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(pk):
+    names = _declared_functions()
+    assert len(names) >= 12
+    L = pk._lib.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    assert sorted(names) == sorted(pk._lib.exported_symbols())
+
+
+def test_block_table_to_csr_reproduces_worked_example(pk):
+    g = json.load(open(os.path.join(GOLDEN, "vllm_worked_example.json")))
+    indptr, indices, last = pk.block_table_to_csr(g["block_table"], g["seq_lens"], g["page_size"])
+    e = g["expect"]
+    assert indptr.tolist() == e["paged_kv_indptr"]
+    assert indices.tolist() == e["paged_kv_indices"]
+    assert last.tolist() == e["paged_kv_last_page_len"]
+
+
+def test_token_table_to_page_table_reproduces_printed_example(pk):
+    g = json.load(open(os.path.join(GOLDEN, "minisgl_metadata_example.json")))
+    pt = pk.token_table_to_page_table(g["token_table"], g["device_len"], 4)
+    assert pt.tolist() == g["expect"]["page_size_4"]["page_table"]
+    # page size 1: the token table itself
+    indptr, indices, last = pk.block_table_to_csr(g["token_table"], g["device_len"], 1)
+    assert indptr.tolist() == g["expect"]["kv_indptr"]
+    assert indices.tolist() == g["expect"]["kv_indices"]
+    assert last.tolist() == g["expect"]["last_page_len"]
+
+
+def _base(**kw):
+    a = dict(qo_indptr=[0, 1, 2], kv_indptr=[0, 2, 3], kv_indices=[3, 1, 0], last_page_len=[5, 16],
+             num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=16, mode="decode", num_sms=152)
+    a.update(kw)
+    return a
+
+
+def _plan(pk, **kw):
+    a = _base(**kw)
+    idx = [a.pop(k) for k in ("qo_indptr", "kv_indptr", "kv_indices", "last_page_len")]
+    return pk.Plan().plan(*idx, host_only=True, **a)
+
+
+@pytest.mark.parametrize("bad, status", [
+    (dict(qo_indptr=[1, 2, 3]), "PKV_EINVAL"),
+    (dict(qo_indptr=[0, 2, 1]), "PKV_EINVAL"),
+    (dict(kv_indptr=[1, 2, 3]), "PKV_EINVAL"),
+    (dict(kv_indptr=[0, 3, 2]), "PKV_EINVAL"),
+    (dict(last_page_len=[0, 16]), "PKV_EINVAL"),
+    (dict(last_page_len=[17, 16]), "PKV_EINVAL"),
+    (dict(kv_indices=[3, -1, 0]), "PKV_EINVAL"),
+    (dict(num_qo_heads=6, num_kv_heads=4), "PKV_EINVAL"),
+    (dict(head_dim=96), "PKV_EUNSUPPORTED"),
+    (dict(qo_indptr=[0, 2, 3]), "PKV_EINVAL"),  # decode mode with two tokens in one request
+    (dict(window_left=-2), "PKV_EINVAL"),
+    (dict(page_size=0), "PKV_EINVAL"),
+    (dict(kv_indptr=[0, 0, 1], kv_indices=[0], last_page_len=[0, 5]), "PKV_EINVAL"),  # a query but no keys
+])
+def test_plan_rejects_invalid_batches(pk, bad, status):
+    with pytest.raises(pk.PkvError) as ei:
+        _plan(pk, **bad)
+    assert ei.value.args[0].startswith(status)
+
+
+def test_run_on_host_only_plan_fails_loudly(pk):
+    import ctypes as C
+
+    p = _plan(pk)
+    cache = pk._lib.pkv_cache(16, 16, 4, 16, 2, 128, 0, 4096, 256, 128, 1.0, 1.0)
+    st = pk._lib.lib().pkv_attn_decode_run(p._h, 16, C.byref(cache), 16, None, None)
+    assert st == pk._lib.PKV_EINVAL
+    assert "host-only" in pk._lib.lib().pkv_last_error().decode()
+
+
+def _check_decode_cover(b, items, window=-1, group=None):
+    """Every (request, kv head, head group) key range [lo, L) is covered once, without overlap."""
+    G = group
+    groups = (G + 15) // 16
+    seen = {}
+    for req, h, hg, k0, k1, q_row, slot, q_rows in items.tolist():
+        assert k0 < k1 and q_rows == 1
+        seen.setdefault((req, h, hg), []).append((k0, k1, slot))
+    for i, L in enumerate(b.kv_len.tolist()):
+        lo = max(0, L - 1 - window) if window >= 0 else 0
+        for h in range(b.num_kv_heads):
+            for hg in range(groups):
+                ranges = sorted(seen.pop((i, h, hg)))
+                assert ranges[0][0] == lo and ranges[-1][1] == L
+                for (a0, a1, s0), (b0, b1, s1) in zip(ranges, ranges[1:]):
+                    assert a1 == b0
+                if len(ranges) == 1:
+                    assert ranges[0][2] == -1
+                else:
+                    slots = sorted(r[2] for r in ranges)
+                    assert slots == list(range(slots[0], slots[0] + len(slots)))
+    assert not seen
+
+
+@pytest.mark.parametrize("n", [2, 4])
+def test_decode_partition_covers_every_key_once(pk, n):
+    import workloads as W
+
+    b = W.workload(n, scale_batch=0.25)
+    p = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=b.num_qo_heads,
+                       num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size, mode="decode",
+                       num_sms=152, host_only=True)
+    items = p.work_items()
+    info = p.info()
+    _check_decode_cover(b, items, group=b.num_qo_heads // b.num_kv_heads)
+    lens = items[:, 4] - items[:, 3]
+    assert np.all(np.diff(lens) <= 0)  # longest first
+    assert info["kv_chunk"] % 64 == 0
+    assert info["num_partials"] == int((items[:, 6] >= 0).sum())
+    assert info["kv_tokens"] == int(b.kv_len.sum())
+
+
+def test_window_partition_and_no_split(pk):
+    import workloads as W
+
+    b = W.make_batch([5000, 70, 4097], [1, 1, 1], 128, 32, 8, 128, seed=1, kv_dtype="e4m3")
+    for w in (4096, 10):
+        p = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
+                           head_dim=128, page_size=128, mode="decode", window_left=w, kv_dtype="e4m3",
+                           num_sms=152, host_only=True)
+        _check_decode_cover(b, p.work_items(), window=w, group=4)
+    p = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
+                       head_dim=128, page_size=128, mode="decode", max_splits=1, kv_dtype="e4m3", num_sms=152,
+                       host_only=True)
+    assert p.info()["num_merge"] == 0 and len(p.work_items()) == 3 * 8
+
+
+def test_large_group_uses_head_groups(pk):
+    import workloads as W
+
+    b = W.make_batch([300, 20], [1, 1], 16, 64, 2, 64, seed=2)
+    p = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=64, num_kv_heads=2,
+                       head_dim=64, page_size=16, mode="decode", num_sms=152, host_only=True)
+    _check_decode_cover(b, p.work_items(), group=32)
+
+
+def test_workspace_size_matches_plan(pk):
+    a = _base()
+    idx = [a.pop(k) for k in ("qo_indptr", "kv_indptr", "kv_indices", "last_page_len")]
+    n = pk.Plan.workspace_size(*idx, **a)
+    p = pk.Plan().plan(*idx, host_only=True, **a)
+    assert p.info()["workspace_bytes"] == n and n % 256 == 0

@@ -175,9 +175,12 @@ WORKLOADS = {
 }
 
 
-def workload(n: int, window_left: int = -1, scale_batch: float = 1.0) -> Batch:
-    """Named workload n (1..5), seed 1000 + n.  ``window_left`` applies to workload 5 only."""
-    seed = 1000 + n
+def workload(n: int, window_left: int = -1, scale_batch: float = 1.0, seed_offset: int = 0) -> Batch:
+    """Named workload n (1..5), seed 1000 + n (+ 100000 * seed_offset, e.g. one batch per rank).
+
+    ``window_left`` applies to workload 5 only; ``scale_batch`` scales the batch size (bounded samples).
+    """
+    seed = 1000 + n + 100000 * int(seed_offset)
     g = torch.Generator(device="cpu").manual_seed(seed + 7919)  # lengths use their own stream
     if n == 1:
         L = [7, 16, 33, 64]
