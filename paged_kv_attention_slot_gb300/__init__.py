@@ -168,14 +168,20 @@ class Plan:
         if host_only:
             check(lib().pkv_attn_plan(self._h, C.byref(a), None, 0, None))
         else:
-            n = C.c_size_t(0)
-            check(lib().pkv_plan_workspace_size(C.byref(a), C.byref(n)))
             if workspace is not None:
                 self.workspace = workspace
-            elif self.workspace is None or self.workspace.numel() < n.value:
-                self.workspace = torch.empty(max(int(n.value), 1 << 16), dtype=torch.uint8, device="cuda")
-            check(lib().pkv_attn_plan(self._h, C.byref(a), self.workspace.data_ptr(), self.workspace.numel(),
-                                      _stream_ptr(stream)))
+            if self.workspace is None:
+                self.workspace = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+            st = lib().pkv_attn_plan(self._h, C.byref(a), self.workspace.data_ptr(), self.workspace.numel(),
+                                     _stream_ptr(stream))
+            if st == _lib.PKV_EWORKSPACE and workspace is None:
+                # grow the binding-owned workspace and plan again
+                n = C.c_size_t(0)
+                check(lib().pkv_plan_workspace_size(C.byref(a), C.byref(n)))
+                self.workspace = torch.empty(int(n.value) + (int(n.value) >> 2), dtype=torch.uint8, device="cuda")
+                st = lib().pkv_attn_plan(self._h, C.byref(a), self.workspace.data_ptr(), self.workspace.numel(),
+                                         _stream_ptr(stream))
+            check(st)
         self.mode = mode
         self.num_qo_heads = num_qo_heads
         self.head_dim = head_dim

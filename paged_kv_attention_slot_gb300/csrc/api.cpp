@@ -93,6 +93,29 @@ int query_num_sms(int32_t requested, int32_t* out) {
   return PKV_OK;
 }
 
+// Order the work list longest first (stable counting sort on the key length, bucketed so that at
+// most 4096 buckets are used: the order is exact up to 1/4096 of the longest key range).
+void order_longest_first(std::vector<WorkItem>& w) {
+  const size_t n = w.size();
+  if (n < 2) return;
+  int32_t maxlen = 0;
+  for (const WorkItem& x : w) maxlen = std::max(maxlen, x.kv_end - x.kv_begin);
+  int shift = 0;
+  while ((maxlen >> shift) >= 4096) ++shift;
+  const int nb = (maxlen >> shift) + 1;
+  thread_local std::vector<uint32_t> count;
+  thread_local std::vector<WorkItem> tmp;
+  count.assign(nb + 1, 0u);
+  tmp.resize(n);
+  uint32_t* c = count.data();
+  const WorkItem* src = w.data();
+  for (size_t i = 0; i < n; ++i) ++c[nb - ((src[i].kv_end - src[i].kv_begin) >> shift)];
+  for (int d = 0; d < nb; ++d) c[d + 1] += c[d];
+  WorkItem* dst = tmp.data();
+  for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - ((src[i].kv_end - src[i].kv_begin) >> shift)]++] = src[i];
+  w.swap(tmp);
+}
+
 // Validate the arguments and build the work list into P (no device work).
 int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   if (!a) return fail(PKV_EINVAL, "args is NULL");
@@ -152,10 +175,18 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
       return fail(PKV_EINVAL, "decode mode allows at most one new token per request (request " + std::to_string(i) + ")");
     P->req[i] = ReqInfo{a->kv_indptr[i], (int32_t)L, a->qo_indptr[i], (int32_t)n};
   }
-  P->indices.assign(a->kv_indices, a->kv_indices + nnz);
-  for (int64_t k = 0; k < nnz; ++k) {
-    if (P->indices[k] < 0) return fail(PKV_EINVAL, "kv_indices entries must be >= 0");
-    P->max_page_id = std::max<int64_t>(P->max_page_id, P->indices[k]);
+  P->indices.resize(nnz);
+  if (nnz) std::memcpy(P->indices.data(), a->kv_indices, nnz * sizeof(int32_t));
+  {
+    int32_t mn = 0, mx = -1;
+    const int32_t* ix = a->kv_indices;
+    if (nnz) mn = mx = ix[0];
+    for (int64_t k = 0; k < nnz; ++k) {
+      mn = std::min(mn, ix[k]);
+      mx = std::max(mx, ix[k]);
+    }
+    if (mn < 0) return fail(PKV_EINVAL, "kv_indices entries must be >= 0");
+    P->max_page_id = nnz ? mx : -1;
   }
 
   int32_t sms = 0;
@@ -183,6 +214,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     const int32_t groups = (G + pkv::kDecodeRows - 1) / pkv::kDecodeRows;
     struct Unit { int32_t req, lo, hi; };
     std::vector<Unit> units;
+    units.reserve(B);
     int64_t total = 0;
     for (int32_t i = 0; i < B; ++i) {
       if (P->req[i].q_len == 0) continue;
@@ -204,37 +236,51 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
       chunk = align_up(chunk, kDecodeChunkAlign);
     }
     P->kv_chunk = chunk;
+    // exact CTA count first, then fill in place
+    int64_t items = 0, merges = 0;
+    for (const Unit& u : units) {
+      const int64_t len = u.hi - u.lo;
+      int64_t ns = (len + chunk - 1) / chunk;
+      if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
+      const int64_t c = align_up((len + ns - 1) / ns, 16);
+      ns = (len + c - 1) / c;
+      items += ns;
+      merges += ns > 1;
+    }
+    const int64_t per_unit = (int64_t)a->num_kv_heads * groups;
+    P->work.resize((size_t)(items * per_unit));
+    P->merge.resize((size_t)(merges * per_unit));
+    WorkItem* wi = P->work.data();
+    MergeItem* mi = P->merge.data();
     int64_t slot = 0;
     for (const Unit& u : units) {
       const int64_t len = u.hi - u.lo;
       int64_t ns = (len + chunk - 1) / chunk;
       if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
-      int64_t c = (len + ns - 1) / ns;
-      c = align_up(c, 16);
+      const int64_t c = align_up((len + ns - 1) / ns, 16);
       ns = (len + c - 1) / c;
+      const int32_t q_row = P->req[u.req].q_begin;
       for (int32_t h = 0; h < a->num_kv_heads; ++h) {
         for (int32_t g = 0; g < groups; ++g) {
-          const int32_t first = ns > 1 ? (int32_t)slot : -1;
           for (int64_t s = 0; s < ns; ++s) {
-            WorkItem w;
+            WorkItem& w = *wi++;
             w.req = u.req;
             w.kv_head = h;
             w.head_group = g;
             w.kv_begin = (int32_t)(u.lo + s * c);
             w.kv_end = (int32_t)std::min<int64_t>(u.hi, u.lo + (s + 1) * c);
-            w.q_row = P->req[u.req].q_begin;
+            w.q_row = q_row;
             w.out_slot = ns > 1 ? (int32_t)(slot + s) : -1;
             w.q_rows = 1;
-            P->work.push_back(w);
           }
           if (ns > 1) {
-            MergeItem m{};
-            m.q_row = P->req[u.req].q_begin;
+            MergeItem& m = *mi++;
+            m = MergeItem{};
+            m.q_row = q_row;
             m.kv_head = h;
             m.head_group = g;
-            m.first_slot = first;
+            m.first_slot = (int32_t)slot;
             m.num_splits = (int32_t)ns;
-            P->merge.push_back(m);
             slot += ns;
           }
         }
@@ -267,9 +313,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     }
   }
   // longest first: the block scheduler hands out CTAs roughly in launch order
-  std::stable_sort(P->work.begin(), P->work.end(), [](const WorkItem& x, const WorkItem& y) {
-    return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
-  });
+  order_longest_first(P->work);
   if ((int64_t)P->work.size() > INT32_MAX) return fail(PKV_EUNSUPPORTED, "too many CTAs");
 
   // workspace layout: [work][merge][req][kv_indices] | [partial lse][partial o]

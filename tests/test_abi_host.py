@@ -139,7 +139,7 @@ def test_decode_partition_covers_every_key_once(pk, n):
     info = p.info()
     _check_decode_cover(b, items, group=b.num_qo_heads // b.num_kv_heads)
     lens = items[:, 4] - items[:, 3]
-    assert np.all(np.diff(lens) <= 0)  # longest first
+    assert np.all(np.diff(lens) <= (lens.max() >> 12) + 1)  # longest first (exact up to 1/4096 of the longest)
     assert info["kv_chunk"] % 64 == 0
     assert info["num_partials"] == int((items[:, 6] >= 0).sum())
     assert info["kv_tokens"] == int(b.kv_len.sum())

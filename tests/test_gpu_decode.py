@@ -178,8 +178,12 @@ def test_decode_plan_reuse_across_layers_and_replan():
     g1.store()
     plan = g1.plan()
     out_a, lse_a = g1.run(plan)
-    # a second "layer": different pool contents, same plan
-    b2 = W.make_batch([70, 300, 20], [1, 1, 1], 16, 8, 2, 128, seed=2)
+    # a second "layer": same batch (page table, slots), different pool contents and queries
+    import dataclasses
+
+    other = W.make_batch([70, 300, 20], [1, 1, 1], 16, 8, 2, 128, seed=2, num_pages=b1.num_pages)
+    b2 = dataclasses.replace(b1, q=other.q, k_new=other.k_new, v_new=other.v_new, k_pool=other.k_pool,
+                             v_pool=other.v_pool)
     g2 = G.GpuBatch(b2)
     g2.store()
     out_b, lse_b = plan.run(g2.q, g2.cache, return_lse=True)
