@@ -1,15 +1,381 @@
-// Causal prefill / prefix-cached extend on tcgen05 tensor cores (work in progress).
+// Causal prefill / prefix-cached extend over a paged KV cache on 5th-generation tensor cores.
+//
+// What it computes: new token t of request i sits at position P = L_i - n_i + t and attends to keys
+// 0..P of the request (bottom-right-aligned causal mask, optional window keeping keys >= P - w),
+// gathered through the request's page list; query head h reads KV head h / G.  The new tokens' own
+// K/V were written into the pool beforehand, so one paged pass covers prefix + new tokens
+// ("vLLM 源码完全拆解（六）：Attention Backend", sections «为什么 KV 写入在 Attention 之前» and «FlashAttention
+// Builder 的结果»: multi-token queries apply the causal mask inside their own request only;
+// "手写 mini-sglang 阶段四 · GPU 注意力后端", section «在 CPU 上验证»: queries are the last n positions).
+//
+// GB300 design (one CTA = 128 query rows x one KV head; rows are (token, head) pairs of the KV
+// head's query-head group, so every K/V tile feeds all G heads):
+//  * warp 4 (producer): Q tile by a 3-D TMA box, then K and V tiles of 128 keys gathered row by row
+//    through the page table with TMA tile::gather4 (4 slot rows per instruction, 128-byte
+//    swizzle), double-buffered, completion counted in bytes on mbarriers;
+//  * warp 5 (MMA): one elected thread issues tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out):
+//    S_j = Q K_j^T into one of two TMEM score buffers, and O += P_{j-1} V_{j-1} into a TMEM output
+//    accumulator, software-pipelined so S_j runs while the softmax works on tile j-1;
+//  * warps 0-3 (softmax): thread r owns query row r = TMEM lane r: tcgen05.ld of its 128 scores,
+//    causal/window mask, online softmax in base 2 with a lazy rescale (the reference maximum only
+//    moves when a row's maximum grows by more than 2^8, the exact trick of keeping numerator and
+//    denominator on one shared reference), P written as bf16 into a swizzled shared tile for the
+//    next MMA, O rescaled in TMEM only when needed, and the final O / l and log-sum-exp.
+// Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its
+// own copies and MMAs, frees its TMEM and exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
 #include "pkv_internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
 
 namespace pkv {
 
-int prefill_supported(const char** why) {
-  if (why) *why = "the prefill kernel is not built yet";
-  return 0;
+int32_t* device_error_ptr();
+
+namespace pf {
+constexpr int ROWS = 128;               // query rows per CTA
+constexpr int KT = 128;                 // keys per K/V tile
+constexpr int D = 128;                  // head dim
+constexpr int HALF_B = ROWS * 128;      // one 64-column half of a 128-row bf16 tile (16 KB)
+constexpr int TILE_B = 2 * HALF_B;      // 32 KB
+constexpr int STAGES = 2;
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILE_B;
+constexpr int OFF_V = OFF_K + STAGES * TILE_B;
+constexpr int OFF_P = OFF_V + STAGES * TILE_B;
+constexpr int OFF_BAR = OFF_P + TILE_B;
+constexpr int NUM_BARS = 17;
+constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_ABORT = OFF_TMEM + 8;
+constexpr int SMEM_USED = OFF_ABORT + 8;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024 bytes
+enum { B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7, B_SF = 9, B_SE = 11, B_PF = 13, B_OD = 14, B_FIN = 15 };
+constexpr uint32_t TMEM_COLS = 512;     // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t TMEM_O = 256;
+constexpr int THREADS = 192;
+constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
+constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
+}  // namespace pf
+
+__global__ void __launch_bounds__(pf::THREADS, 1)
+    prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, int32_t* err) {
+  using namespace pf;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t base = (raw_u + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw_u);
+  const uint32_t sQ = base + OFF_Q, sK = base + OFF_K, sV = base + OFF_V, sP = base + OFF_P;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + OFF_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + OFF_TMEM);
+#define BAR(i) (base + OFF_BAR + 8u * (uint32_t)(i))
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WorkItem w = p.work[blockIdx.x];
+  const ReqInfo ri = p.req[w.req];
+  const int G = p.group;
+  const int nkt = (w.kv_end - w.kv_begin + KT - 1) / KT;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    tc::mbar_init(BAR(B_Q), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(BAR(B_KF + s), 1);
+      tc::mbar_init(BAR(B_VF + s), 1);
+      tc::mbar_init(BAR(B_KE + s), 1);
+      tc::mbar_init(BAR(B_VE + s), 1);
+      tc::mbar_init(BAR(B_SF + s), 1);
+      tc::mbar_init(BAR(B_SE + s), 4);
+    }
+    tc::mbar_init(BAR(B_PF), 4);
+    tc::mbar_init(BAR(B_OD), 1);
+    tc::mbar_init(BAR(B_FIN), 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------------ producer (TMA)
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tq);
+      tc::tma_prefetch_desc(&tk);
+      tc::tma_prefetch_desc(&tv);
+      tc::mbar_arrive_expect_tx(BAR(B_Q), TILE_B);
+      tc::tma_load_3d(sQ, &tq, BAR(B_Q), 0, w.kv_head * G, w.q_row);
+      tc::tma_load_3d(sQ + HALF_B, &tq, BAR(B_Q), 64, w.kv_head * G, w.q_row);
+    }
+    const int col0 = w.kv_head * D;
+    int issued = 0;  // tiles whose K and V copies were issued
+    bool ok = true;
+    for (int j = 0; j < nkt && ok; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      int rows[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        int key = w.kv_begin + j * KT + 4 * lane + q;
+        if (key >= w.kv_end) key = w.kv_end - 1;  // clamp the tail to a valid row; it is masked later
+        const int lp = key / p.page_size;
+        const int off = key - lp * p.page_size;
+        const int page = __ldg(p.kv_indices + ri.page_base + lp);
+        if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages) {
+          record_error(err, PKV_DEVERR_PAGE_RANGE);
+          rows[q] = 0;
+        } else {
+          rows[q] = page * p.page_size + off;
+        }
+      }
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_KE + st), ph ^ 1, abort_flag, WAIT_LIMIT));
+      if (!ok) break;
+      if (lane == 0) tc::mbar_arrive_expect_tx(BAR(B_KF + st), TILE_B);
+      __syncwarp();
+      const uint32_t dk = sK + st * TILE_B + (4 * lane) * 128;
+      tc::tma_gather4(dk, &tk, BAR(B_KF + st), col0, rows[0], rows[1], rows[2], rows[3]);
+      tc::tma_gather4(dk + HALF_B, &tk, BAR(B_KF + st), col0 + 64, rows[0], rows[1], rows[2], rows[3]);
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_VE + st), ph ^ 1, abort_flag, WAIT_LIMIT));
+      if (!ok) {
+        issued = j;  // K of tile j is in flight, V is not
+        break;
+      }
+      if (lane == 0) tc::mbar_arrive_expect_tx(BAR(B_VF + st), TILE_B);
+      __syncwarp();
+      const uint32_t dv = sV + st * TILE_B + (4 * lane) * 128;
+      tc::tma_gather4(dv, &tv, BAR(B_VF + st), col0, rows[0], rows[1], rows[2], rows[3]);
+      tc::tma_gather4(dv + HALF_B, &tv, BAR(B_VF + st), col0 + 64, rows[0], rows[1], rows[2], rows[3]);
+      issued = j + 1;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
+      // let the copies already in flight land before the CTA's shared memory goes away
+      volatile int never = 0;
+      for (int j = (issued > 2 ? issued - 2 : 0); j <= issued && j < nkt; ++j) {
+        tc::mbar_wait(BAR(B_KF + (j & 1)), (j >> 1) & 1, &never, WAIT_LIMIT / 8);
+        if (j < issued) tc::mbar_wait(BAR(B_VF + (j & 1)), (j >> 1) & 1, &never, WAIT_LIMIT / 8);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, KT, false);
+      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, true);
+      bool ok = tc::mbar_wait(BAR(B_Q), 0, abort_flag, WAIT_LIMIT);
+      tc::fence_after_sync();
+      for (int j = 0; j <= nkt && ok; ++j) {
+        if (j < nkt) {
+          const int st = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          ok = tc::mbar_wait(BAR(B_KF + st), ph, abort_flag, WAIT_LIMIT) &&
+               tc::mbar_wait(BAR(B_SE + st), ph ^ 1, abort_flag, WAIT_LIMIT);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t d = tmem + (uint32_t)st * KT;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * HALF_B + (ks & 3) * 32;
+            const uint64_t a = tc::smem_desc_sw128(sQ + off, 16, 1024);
+            const uint64_t b = tc::smem_desc_sw128(sK + st * TILE_B + off, 16, 1024);
+            tc::mma_bf16_ss(d, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+          }
+          tc::commit(BAR(B_SF + st));
+          tc::commit(BAR(B_KE + st));
+        }
+        if (j >= 1) {
+          const int jp = j - 1;
+          const int st = jp & 1;
+          const uint32_t ph = (jp >> 1) & 1;
+          ok = tc::mbar_wait(BAR(B_PF), jp & 1, abort_flag, WAIT_LIMIT) &&
+               tc::mbar_wait(BAR(B_VF + st), ph, abort_flag, WAIT_LIMIT);
+          if (!ok) break;
+          tc::fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < KT / 16; ++kk) {
+            const uint64_t a = tc::smem_desc_sw128(sP + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+            const uint64_t b = tc::smem_desc_sw128(sV + st * TILE_B + kk * 2048, HALF_B, 1024);
+            tc::mma_bf16_ss(tmem + TMEM_O, a, b, idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit(BAR(B_OD));
+          tc::commit(BAR(B_VE + st));
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(err, PKV_DEVERR_TIMEOUT);
+        // every MMA issued so far must be complete before the TMEM is freed
+        tc::commit(BAR(B_FIN));
+        volatile int never = 0;
+        tc::mbar_wait(BAR(B_FIN), 0, &never, WAIT_LIMIT / 8);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax (warps 0-3)
+    const int r = threadIdx.x;  // query row == TMEM lane
+    const int t = r / G;
+    const int g = r - t * G;
+    const bool row_valid = t < w.q_rows;
+    const int pos0 = ri.kv_len - ri.q_len + (w.q_row - ri.q_begin);  // position of the tile's first token
+    const int P = pos0 + min(t, w.q_rows - 1);
+    const int lo = p.window_left >= 0 ? max(0, P - p.window_left) : 0;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float sc = p.scale_log2;
+    float m_used = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkt; ++j) {
+      const int sb = j & 1;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_SF + sb), (j >> 1) & 1, abort_flag, WAIT_LIMIT));
+      if (!ok) break;
+      tc::fence_after_sync();
+      float x[KT];
+#pragma unroll
+      for (int c4 = 0; c4 < KT / 32; ++c4) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + lane_base + (uint32_t)sb * KT + c4 * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[c4 * 32 + i] = __uint_as_float(v[i]);
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(BAR(B_SE + sb));
+
+      // scale, mask, row maximum (log2 units)
+      const int k0 = w.kv_begin + j * KT;
+      const bool full = (k0 + KT - 1 <= P) && (k0 >= lo);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < KT; ++c) {
+        float xv = x[c] * sc;
+        if (!full) {
+          const int kk = k0 + c;
+          if (kk > P || kk < lo) xv = -INFINITY;
+        }
+        x[c] = xv;
+        mx = fmaxf(mx, xv);
+      }
+      float corr = 1.f;
+      bool rescale = false;
+      if (mx > m_used + RESCALE_THRESHOLD) {
+        corr = ex2(m_used - mx);  // 0 on the first visible tile
+        m_used = mx;
+        l *= corr;
+        rescale = true;
+      }
+      const float mref = m_used == -INFINITY ? 0.f : m_used;
+      float sum = 0.f;
+      uint32_t pk[KT / 2];
+#pragma unroll
+      for (int c = 0; c < KT / 2; ++c) {
+        const float p0 = ex2(x[2 * c] - mref);
+        const float p1 = ex2(x[2 * c + 1] - mref);
+        sum += p0 + p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      l += sum;
+
+      // PV of the previous tile must be complete: O is stable and the P buffer is free
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD), (j - 1) & 1, abort_flag, WAIT_LIMIT));
+        if (!ok) break;
+        tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t v[32];
+            const uint32_t ta = tmem + lane_base + TMEM_O + c4 * 32;
+            tc::tmem_ld32(ta, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+            tc::tmem_st32(ta, v);
+          }
+        }
+      }
+      // P row -> swizzled K-major bf16 tile (two 64-key halves)
+#pragma unroll
+      for (int c16 = 0; c16 < KT / 8; ++c16) {
+        const int half = c16 >> 3, ch = c16 & 7;
+        const uint32_t addr = sP + half * HALF_B + r * 128 + ((ch ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(pk[4 * c16]),
+                     "r"(pk[4 * c16 + 1]), "r"(pk[4 * c16 + 2]), "r"(pk[4 * c16 + 3])
+                     : "memory");
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(BAR(B_PF));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD), (nkt - 1) & 1, abort_flag, WAIT_LIMIT));
+    if (ok) {
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int head = w.kv_head * G + g;
+      const int64_t row = (int64_t)(w.q_row + t);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D);
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + lane_base + TMEM_O + c4 * 32, v);
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
+            u.y = pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
+            u.z = pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
+            u.w = pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
+            dst[c4 * 4 + q] = u;
+          }
+        }
+      }
+      if (row_valid && p.lse) p.lse[row * p.num_qo_heads + head] = (m_used + __log2f(l)) * 0.69314718055994531f;
+    } else {
+      *abort_flag = 1;
+      if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+#undef BAR
 }
 
-cudaError_t launch_prefill(const RunParams&, const void*, const void*, const void*, int64_t, cudaStream_t) {
-  return cudaErrorNotSupported;
+int prefill_supported(const char** why) {
+  if (why) *why = nullptr;
+  return 1;
+}
+
+cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v, int64_t,
+                           cudaStream_t s) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, pf::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int32_t* err = device_error_ptr();
+  if (!err) return cudaErrorInvalidDevice;
+  prefill_kernel<<<(unsigned)p.num_work, pf::THREADS, pf::SMEM_ALLOC, s>>>(
+      p, *static_cast<const CUtensorMap*>(tmap_q), *static_cast<const CUtensorMap*>(tmap_k),
+      *static_cast<const CUtensorMap*>(tmap_v), err);
+  return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -1,0 +1,81 @@
+"""GPU parity of causal prefill / prefix-cached extend (tcgen05 kernel) against the CPU oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import gpu_common as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import paged_kv_attention_slot_gb300 as pk
+
+    pk._lib.lib()
+    assert pk.device_error() == 0
+    yield
+    assert pk.device_error() == 0
+
+
+def _case(b, rows=None, **plan_kw):
+    g = G.GpuBatch(b)
+    g.store()
+    plan = g.plan(**plan_kw)
+    out, lse = g.run(plan)
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt, rows=rows)
+    return G.compare(out, lse, ro, rl, rows=rows), plan
+
+
+def test_prefill_single_tile_no_prefix():
+    # one request, 32 new tokens, no cached prefix, G = 4: exactly one 128-row tile and one K tile
+    b = W.make_batch([32], [32], 1, 8, 2, 128, seed=1)
+    _case(b)
+
+
+def test_prefill_multi_tile_with_prefix():
+    b = W.make_batch([300], [70], 1, 8, 2, 128, seed=2)
+    _case(b)
+
+
+@pytest.mark.parametrize("hq, hkv", [(4, 4), (8, 4), (8, 2), (16, 2), (32, 2)])
+def test_prefill_gqa_groups(hq, hkv):
+    b = W.make_batch([129, 50, 400], [129, 17, 260], 1, hq, hkv, 128, seed=hq + hkv)
+    _case(b)
+
+
+@pytest.mark.parametrize("ps", [1, 4, 16, 64])
+def test_prefill_page_sizes(ps):
+    b = W.make_batch([1, 40, 257, 700], [1, 33, 200, 129], ps, 8, 2, 128, seed=10 + ps)
+    _case(b)
+
+
+def test_prefill_ragged_with_idle_requests():
+    b = W.make_batch([90, 0, 13, 1000, 5], [0, 0, 13, 3, 5], 1, 16, 4, 128, seed=5)
+    _case(b)
+
+
+@pytest.mark.parametrize("window", [0, 7, 128, 300])
+def test_prefill_sliding_window(window):
+    b = W.make_batch([600, 140, 33], [200, 140, 1], 1, 8, 2, 128, seed=20 + window, window_left=window)
+    _case(b)
+
+
+def test_prefill_custom_scale_large_scores():
+    # a large softmax scale stresses the lazy rescaling of the running maximum
+    b = W.make_batch([512, 700], [256, 700], 1, 8, 2, 128, seed=7, sm_scale=1.5)
+    _case(b)
+
+
+def test_prefill_full_size_prefix_extend_sampled():
+    b = W.workload(3)
+    rng = np.random.default_rng(3)
+    rows = []
+    for i in range(b.batch_size):
+        q0, q1 = int(b.qo_indptr[i]), int(b.qo_indptr[i + 1])
+        rows += [q0, q1 - 1] + rng.integers(q0, q1, size=3).tolist()
+    stats, plan = _case(b, rows=sorted(set(rows)))
+    assert plan.info()["num_work"] > 1000
