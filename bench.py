@@ -367,6 +367,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--only-prefill", action="store_true", help="measure the prefill workload alone (profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -376,6 +377,17 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, world, rank)
+    if args.only_prefill:
+        import torch
+
+        import paged_kv_attention_slot_gb300 as pk
+
+        torch.cuda.set_device(local_rank)
+        pk._lib.lib()
+        res = prefill_measure(torch.device("cuda", local_rank), args.steps, args.warmup, _peaks()[1])
+        res["device_error"] = pk.device_error()
+        print(json.dumps(res))
+        return
 
     import torch
 
