@@ -10,10 +10,14 @@
 //
 // GB300 design (one CTA = 128 query rows x one KV head; rows are (token, head) pairs of the KV
 // head's query-head group, so every K/V tile feeds all G heads):
-//  * warp 4 (producer): Q tile by a 3-D TMA box, then K and V tiles of 128 keys gathered row by row
-//    through the page table with TMA tile::gather4 (4 slot rows per instruction, 128-byte
-//    swizzle), double-buffered, completion counted in bytes on mbarriers;
-//  * warp 5 (MMA): one elected thread issues tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out):
+//  * warps 5-8 (producers): the Q tile by one 3-D TMA box; K (warps 5-6) and V (warps 7-8) tiles of
+//    128 keys gathered row by row through the page table with 16-byte cp.async, 16 lanes per
+//    256-byte row (fully coalesced), written straight into the 128-byte-swizzled K-major layout
+//    the tensor core reads, double-buffered; each producer thread waits for its own copies, fences
+//    them into the async proxy and arrives on the stage's mbarrier.  (TMA tile::gather4 moves only
+//    512 bytes per instruction; issued one lane at a time it was the bottleneck for token-granular
+//    pools, which is why the rows go through cp.async instead);
+//  * warp 4 (MMA): one elected thread issues tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out):
 //    S_j = Q K_j^T into one of two TMEM score buffers, and O += P_{j-1} V_{j-1} into a TMEM output
 //    accumulator, software-pipelined so S_j runs while the softmax works on tile j-1;
 //  * warps 0-3 (softmax): thread r owns query row r = TMEM lane r: tcgen05.ld of its 128 scores,
@@ -56,7 +60,8 @@ constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024 
 enum { B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7, B_SF = 9, B_SE = 11, B_PF = 13, B_OD = 14, B_FIN = 15 };
 constexpr uint32_t TMEM_COLS = 512;     // S0 [0,128), S1 [128,256), O [256,384)
 constexpr uint32_t TMEM_O = 256;
-constexpr int THREADS = 192;
+constexpr int THREADS = 288;  // 4 softmax warps, 1 MMA warp, 2 K-producer warps, 2 V-producer warps
+constexpr int PRODUCER_THREADS = 64;  // per operand (K or V)
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 }  // namespace pf
@@ -85,8 +90,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     *abort_flag = 0;
     tc::mbar_init(BAR(B_Q), 1);
     for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(BAR(B_KF + s), 1);
-      tc::mbar_init(BAR(B_VF + s), 1);
+      tc::mbar_init(BAR(B_KF + s), PRODUCER_THREADS);
+      tc::mbar_init(BAR(B_VF + s), PRODUCER_THREADS);
       tc::mbar_init(BAR(B_KE + s), 1);
       tc::mbar_init(BAR(B_VE + s), 1);
       tc::mbar_init(BAR(B_SF + s), 1);
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc::mbar_init(BAR(B_FIN), 1);
     tc::mbar_fence_init();
   }
-  if (warp == 5) {
+  if (warp == 4) {
     tc::tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -106,67 +111,72 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------------ producer (TMA)
-    if (lane == 0) {
+  if (warp >= 5) {
+    // ------------------------------------------------------------------ producers (cp.async)
+    const bool is_k = warp < 7;
+    const int pw = (warp - 5) & 1;  // which 64-row half of the tile this warp fills
+    const char* pool = is_k ? p.k_pool : p.v_pool;
+    const uint32_t s_base = is_k ? sK : sV;
+    const uint32_t full0 = is_k ? BAR(B_KF) : BAR(B_VF);
+    const uint32_t empty0 = is_k ? BAR(B_KE) : BAR(B_VE);
+    if (warp == 5 && lane == 0) {
       tc::tma_prefetch_desc(&tq);
-      tc::tma_prefetch_desc(&tk);
-      tc::tma_prefetch_desc(&tv);
       tc::mbar_arrive_expect_tx(BAR(B_Q), TILE_B);
       tc::tma_load_3d(sQ, &tq, BAR(B_Q), 0, w.kv_head * G, w.q_row);
       tc::tma_load_3d(sQ + HALF_B, &tq, BAR(B_Q), 64, w.kv_head * G, w.q_row);
     }
-    const int col0 = w.kv_head * D;
-    int issued = 0;  // tiles whose K and V copies were issued
+    const int64_t head_off = (int64_t)w.kv_head * p.stride_head_b;
+    const int c = lane & 15;  // 16-byte chunk of the 256-byte row
+    const int half = c >> 3, cc = c & 7;
+    auto slot_of = [&](int key) -> int {
+      if (key >= w.kv_end) return -1;
+      const int lp = key / p.page_size;
+      const int page = __ldg(p.kv_indices + ri.page_base + lp);
+      if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages) {
+        record_error(err, PKV_DEVERR_PAGE_RANGE);
+        return -1;
+      }
+      return page * p.page_size + (key - lp * p.page_size);
+    };
     bool ok = true;
+    int pending = 0;  // tiles issued whose arrival is still owed
     for (int j = 0; j < nkt && ok; ++j) {
       const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      int rows[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        int key = w.kv_begin + j * KT + 4 * lane + q;
-        if (key >= w.kv_end) key = w.kv_end - 1;  // clamp the tail to a valid row; it is masked later
-        const int lp = key / p.page_size;
-        const int off = key - lp * p.page_size;
-        const int page = __ldg(p.kv_indices + ri.page_base + lp);
-        if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages) {
-          record_error(err, PKV_DEVERR_PAGE_RANGE);
-          rows[q] = 0;
-        } else {
-          rows[q] = page * p.page_size + off;
-        }
-      }
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_KE + st), ph ^ 1, abort_flag, WAIT_LIMIT));
+      const int key0 = w.kv_begin + j * KT + pw * 64;
+      const int slot_a = slot_of(key0 + lane);
+      const int slot_b = slot_of(key0 + 32 + lane);
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, WAIT_LIMIT));
       if (!ok) break;
-      if (lane == 0) tc::mbar_arrive_expect_tx(BAR(B_KF + st), TILE_B);
-      __syncwarp();
-      const uint32_t dk = sK + st * TILE_B + (4 * lane) * 128;
-      tc::tma_gather4(dk, &tk, BAR(B_KF + st), col0, rows[0], rows[1], rows[2], rows[3]);
-      tc::tma_gather4(dk + HALF_B, &tk, BAR(B_KF + st), col0 + 64, rows[0], rows[1], rows[2], rows[3]);
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_VE + st), ph ^ 1, abort_flag, WAIT_LIMIT));
-      if (!ok) {
-        issued = j;  // K of tile j is in flight, V is not
-        break;
+      const uint32_t dst0 = s_base + st * TILE_B + half * HALF_B;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int rr = 2 * i + (lane >> 4);  // row within this warp's 64
+        const int slot = __shfl_sync(0xffffffffu, i < 16 ? slot_a : slot_b, rr & 31);
+        const int row = pw * 64 + rr;
+        const uint32_t dst = dst0 + row * 128 + ((cc ^ (row & 7)) << 4);
+        const char* src = pool + (slot >= 0 ? (int64_t)slot * p.stride_token_b + head_off + c * 16 : 0);
+        cp_async16(dst, src, slot >= 0 ? 16u : 0u);
       }
-      if (lane == 0) tc::mbar_arrive_expect_tx(BAR(B_VF + st), TILE_B);
-      __syncwarp();
-      const uint32_t dv = sV + st * TILE_B + (4 * lane) * 128;
-      tc::tma_gather4(dv, &tv, BAR(B_VF + st), col0, rows[0], rows[1], rows[2], rows[3]);
-      tc::tma_gather4(dv + HALF_B, &tv, BAR(B_VF + st), col0 + 64, rows[0], rows[1], rows[2], rows[3]);
-      issued = j + 1;
+      cp_async_commit();
+      ++pending;
+      if (j > 0) {
+        // this thread's copies of tile j-1 have landed: publish them to the tensor core
+        cp_async_wait<1>();
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(full0 + 8 * ((j - 1) & 1));
+        --pending;
+      }
+    }
+    cp_async_wait<0>();
+    if (pending > 0 && ok) {
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(full0 + 8 * ((nkt - 1) & 1));
     }
     if (!ok) {
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
-      // let the copies already in flight land before the CTA's shared memory goes away
-      volatile int never = 0;
-      for (int j = (issued > 2 ? issued - 2 : 0); j <= issued && j < nkt; ++j) {
-        tc::mbar_wait(BAR(B_KF + (j & 1)), (j >> 1) & 1, &never, WAIT_LIMIT / 8);
-        if (j < issued) tc::mbar_wait(BAR(B_VF + (j & 1)), (j >> 1) & 1, &never, WAIT_LIMIT / 8);
-      }
     }
-  } else if (warp == 5) {
+  } else if (warp == 4) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, KT, false);
@@ -180,6 +190,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           ok = tc::mbar_wait(BAR(B_KF + st), ph, abort_flag, WAIT_LIMIT) &&
                tc::mbar_wait(BAR(B_SE + st), ph ^ 1, abort_flag, WAIT_LIMIT);
           if (!ok) break;
+          tc::fence_proxy_async_smem();
           tc::fence_after_sync();
           const uint32_t d = tmem + (uint32_t)st * KT;
 #pragma unroll
@@ -199,6 +210,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           ok = tc::mbar_wait(BAR(B_PF), jp & 1, abort_flag, WAIT_LIMIT) &&
                tc::mbar_wait(BAR(B_VF + st), ph, abort_flag, WAIT_LIMIT);
           if (!ok) break;
+          tc::fence_proxy_async_smem();
           tc::fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk) {
@@ -254,17 +266,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // scale, mask, row maximum (log2 units)
       const int k0 = w.kv_begin + j * KT;
       const bool full = (k0 + KT - 1 <= P) && (k0 >= lo);
-      float mx = -INFINITY;
+      float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const int hi_c = P - k0, lo_c = lo - k0;  // visible columns: lo_c <= c <= hi_c
 #pragma unroll
       for (int c = 0; c < KT; ++c) {
         float xv = x[c] * sc;
-        if (!full) {
-          const int kk = k0 + c;
-          if (kk > P || kk < lo) xv = -INFINITY;
-        }
+        if (!full && (c > hi_c || c < lo_c)) xv = -INFINITY;
         x[c] = xv;
-        mx = fmaxf(mx, xv);
+        mxa[c & 3] = fmaxf(mxa[c & 3], xv);
       }
+      const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
       float corr = 1.f;
       bool rescale = false;
       if (mx > m_used + RESCALE_THRESHOLD) {
@@ -274,16 +285,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         rescale = true;
       }
       const float mref = m_used == -INFINITY ? 0.f : m_used;
-      float sum = 0.f;
+      float sa[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[KT / 2];
 #pragma unroll
       for (int c = 0; c < KT / 2; ++c) {
         const float p0 = ex2(x[2 * c] - mref);
         const float p1 = ex2(x[2 * c + 1] - mref);
-        sum += p0 + p1;
+        sa[c & 3] += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
       }
-      l += sum;
+      l += (sa[0] + sa[1]) + (sa[2] + sa[3]);
 
       // PV of the previous tile must be complete: O is stable and the P buffer is free
       if (j > 0) {
@@ -348,7 +359,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 4) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }
