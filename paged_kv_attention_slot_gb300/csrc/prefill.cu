@@ -10,21 +10,24 @@
 //
 // GB300 design (one CTA = 128 query rows x one KV head; rows are (token, head) pairs of the KV
 // head's query-head group, so every K/V tile feeds all G heads):
-//  * warps 5-8 (producers): the Q tile by one 3-D TMA box; K (warps 5-6) and V (warps 7-8) tiles of
+//  * warps 9-12 (producers): the Q tile by one 3-D TMA box; K (warps 9-10) and V (warps 11-12) tiles of
 //    128 keys gathered row by row through the page table with 16-byte cp.async, 16 lanes per
 //    256-byte row (fully coalesced), written straight into the 128-byte-swizzled K-major layout
 //    the tensor core reads, double-buffered; each producer thread waits for its own copies, fences
 //    them into the async proxy and arrives on the stage's mbarrier.  (TMA tile::gather4 moves only
 //    512 bytes per instruction; issued one lane at a time it was the bottleneck for token-granular
 //    pools, which is why the rows go through cp.async instead);
-//  * warp 4 (MMA): one elected thread issues tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out):
+//  * warp 8 (MMA): one elected thread issues tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out):
 //    S_j = Q K_j^T into one of two TMEM score buffers, and O += P_{j-1} V_{j-1} into a TMEM output
 //    accumulator, software-pipelined so S_j runs while the softmax works on tile j-1;
-//  * warps 0-3 (softmax): thread r owns query row r = TMEM lane r: tcgen05.ld of its 128 scores,
-//    causal/window mask, online softmax in base 2 with a lazy rescale (the reference maximum only
-//    moves when a row's maximum grows by more than 2^8, the exact trick of keeping numerator and
-//    denominator on one shared reference), P written as bf16 into a swizzled shared tile for the
-//    next MMA, O rescaled in TMEM only when needed, and the final O / l and log-sum-exp.
+//  * warps 0-7 (softmax): warp w owns query rows 32 (w % 4) .. +31 (= its TMEM lanes) and key
+//    columns 64 (w / 4) .. +63 of every tile: one tcgen05.ld of its 64 scores, causal/window mask on
+//    diagonal tiles only, row maximum shared with the partner warp of the other column half through
+//    shared memory and a 2-arrival mbarrier (bounded wait), online softmax in base 2 with the score scale
+//    folded into one FFMA before ex2, and a lazy rescale (the reference maximum only moves when a
+//    row's maximum grows by more than 2^8, exact because numerator and denominator share the
+//    reference); P written as bf16 into a swizzled shared tile for the next MMA, O rescaled in TMEM
+//    only when needed, then the final O / l and log-sum-exp.
 // Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its
 // own copies and MMAs, frees its TMEM and exits.
 
@@ -52,15 +55,23 @@ constexpr int OFF_K = OFF_Q + TILE_B;
 constexpr int OFF_V = OFF_K + STAGES * TILE_B;
 constexpr int OFF_P = OFF_V + STAGES * TILE_B;
 constexpr int OFF_BAR = OFF_P + TILE_B;
-constexpr int NUM_BARS = 17;
+constexpr int NUM_BARS = 32;
 constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
-constexpr int SMEM_USED = OFF_ABORT + 8;
+constexpr int OFF_XCH = OFF_ABORT + 8;               // row-max exchange [2 tiles][2 halves][128] + sums
+constexpr int SMEM_USED = OFF_XCH + (2 * 2 * 128 + 2 * 128) * 4;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024 bytes
-enum { B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7, B_SF = 9, B_SE = 11, B_PF = 13, B_OD = 14, B_FIN = 15 };
+enum {
+  B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7, B_SF = 9, B_SE = 11, B_PF = 13, B_OD = 14, B_FIN = 15,
+  B_XM = 16,  // [4 row quarters][2 tile parities]: the two column-half warps exchanged their maxima
+  B_XL = 24   // [4 row quarters]: the two column-half warps exchanged their final row sums
+};
 constexpr uint32_t TMEM_COLS = 512;     // S0 [0,128), S1 [128,256), O [256,384)
 constexpr uint32_t TMEM_O = 256;
-constexpr int THREADS = 288;  // 4 softmax warps, 1 MMA warp, 2 K-producer warps, 2 V-producer warps
+constexpr int THREADS = 416;  // 8 softmax warps, 1 MMA warp, 2 K-producer warps, 2 V-producer warps
+constexpr int SOFTMAX_WARPS = 8;
+constexpr int MMA_WARP = 8;
+constexpr int PRODUCER_WARP0 = 9;
 constexpr int PRODUCER_THREADS = 64;  // per operand (K or V)
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
@@ -95,14 +106,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       tc::mbar_init(BAR(B_KE + s), 1);
       tc::mbar_init(BAR(B_VE + s), 1);
       tc::mbar_init(BAR(B_SF + s), 1);
-      tc::mbar_init(BAR(B_SE + s), 4);
+      tc::mbar_init(BAR(B_SE + s), SOFTMAX_WARPS);
     }
-    tc::mbar_init(BAR(B_PF), 4);
+    tc::mbar_init(BAR(B_PF), SOFTMAX_WARPS);
     tc::mbar_init(BAR(B_OD), 1);
     tc::mbar_init(BAR(B_FIN), 1);
+    for (int i = 0; i < 8; ++i) tc::mbar_init(BAR(B_XM + i), 2);
+    for (int i = 0; i < 4; ++i) tc::mbar_init(BAR(B_XL + i), 2);
     tc::mbar_fence_init();
   }
-  if (warp == 4) {
+  if (warp == MMA_WARP) {
     tc::tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -111,15 +124,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 5) {
+  if (warp >= PRODUCER_WARP0) {
     // ------------------------------------------------------------------ producers (cp.async)
-    const bool is_k = warp < 7;
-    const int pw = (warp - 5) & 1;  // which 64-row half of the tile this warp fills
+    const bool is_k = warp < PRODUCER_WARP0 + 2;
+    const int pw = (warp - PRODUCER_WARP0) & 1;  // which 64-row half of the tile this warp fills
     const char* pool = is_k ? p.k_pool : p.v_pool;
     const uint32_t s_base = is_k ? sK : sV;
     const uint32_t full0 = is_k ? BAR(B_KF) : BAR(B_VF);
     const uint32_t empty0 = is_k ? BAR(B_KE) : BAR(B_VE);
-    if (warp == 5 && lane == 0) {
+    if (warp == PRODUCER_WARP0 && lane == 0) {
       tc::tma_prefetch_desc(&tq);
       tc::mbar_arrive_expect_tx(BAR(B_Q), TILE_B);
       tc::tma_load_3d(sQ, &tq, BAR(B_Q), 0, w.kv_head * G, w.q_row);
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp == 4) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, KT, false);
@@ -233,49 +246,58 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ softmax (warps 0-3)
-    const int r = threadIdx.x;  // query row == TMEM lane
+    // ------------------------------------------------------------------ softmax (warps 0-7)
+    const int quarter = warp & 3;
+    const int ch = warp >> 2;                 // key-column half of every tile
+    const int r = quarter * 32 + lane;        // query row == TMEM lane
     const int t = r / G;
     const int g = r - t * G;
     const bool row_valid = t < w.q_rows;
     const int pos0 = ri.kv_len - ri.q_len + (w.q_row - ri.q_begin);  // position of the tile's first token
     const int P = pos0 + min(t, w.q_rows - 1);
     const int lo = p.window_left >= 0 ? max(0, P - p.window_left) : 0;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t col_half = (uint32_t)ch * 64;
     const float sc = p.scale_log2;
+    float* xch = reinterpret_cast<float*>(sbase + OFF_XCH);  // [2][2][128] maxima, then [2][128] sums
     float m_used = -INFINITY;
-    float l = 0.f;
+    float l = 0.f;  // this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
       const int sb = j & 1;
       ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_SF + sb), (j >> 1) & 1, abort_flag, WAIT_LIMIT));
       if (!ok) break;
       tc::fence_after_sync();
-      float x[KT];
-#pragma unroll
-      for (int c4 = 0; c4 < KT / 32; ++c4) {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + lane_base + (uint32_t)sb * KT + c4 * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c4 * 32 + i] = __uint_as_float(v[i]);
-      }
+      uint32_t v[64];
+      tc::tmem_ld64(tmem + lane_base + (uint32_t)sb * KT + col_half, v);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(BAR(B_SE + sb));
 
-      // scale, mask, row maximum (log2 units)
-      const int k0 = w.kv_begin + j * KT;
-      const bool full = (k0 + KT - 1 <= P) && (k0 >= lo);
-      float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // raw-score maximum over the visible columns of this half (the scale is positive)
+      const int k0 = w.kv_begin + j * KT + ch * 64;
       const int hi_c = P - k0, lo_c = lo - k0;  // visible columns: lo_c <= c <= hi_c
+      const bool full = __all_sync(0xffffffffu, hi_c >= 63 && lo_c <= 0);
+      float ma[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < KT; ++c) {
-        float xv = x[c] * sc;
-        if (!full && (c > hi_c || c < lo_c)) xv = -INFINITY;
-        x[c] = xv;
-        mxa[c & 3] = fmaxf(mxa[c & 3], xv);
+        for (int c = 0; c < 64; ++c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          if (c > hi_c || c < lo_c) v[c] = __float_as_uint(-INFINITY);
+          ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
+        }
       }
-      const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+      float mx = fmaxf(fmaxf(ma[0], ma[1]), fmaxf(ma[2], ma[3])) * sc;
+      // share the maximum with the partner warp holding the other 64 columns of the same rows
+      xch[(sb * 2 + ch) * 128 + r] = mx;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(BAR(B_XM + quarter * 2 + sb));
+      ok = __all_sync(0xffffffffu,
+                      tc::mbar_wait(BAR(B_XM + quarter * 2 + sb), (j >> 1) & 1, abort_flag, WAIT_LIMIT));
+      if (!ok) break;
+      mx = fmaxf(mx, xch[(sb * 2 + (ch ^ 1)) * 128 + r]);
       float corr = 1.f;
       bool rescale = false;
       if (mx > m_used + RESCALE_THRESHOLD) {
@@ -284,13 +306,13 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         l *= corr;
         rescale = true;
       }
-      const float mref = m_used == -INFINITY ? 0.f : m_used;
+      const float nref = m_used == -INFINITY ? 0.f : -m_used;
       float sa[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[KT / 2];
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < KT / 2; ++c) {
-        const float p0 = ex2(x[2 * c] - mref);
-        const float p1 = ex2(x[2 * c + 1] - mref);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(__uint_as_float(v[2 * c]), sc, nref));
+        const float p1 = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sc, nref));
         sa[c & 3] += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
       }
@@ -303,23 +325,22 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         tc::fence_after_sync();
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t v[32];
-            const uint32_t ta = tmem + lane_base + TMEM_O + c4 * 32;
-            tc::tmem_ld32(ta, v);
+          for (int c4 = 0; c4 < 2; ++c4) {
+            uint32_t o[32];
+            const uint32_t ta = tmem + lane_base + TMEM_O + col_half + c4 * 32;
+            tc::tmem_ld32(ta, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-            tc::tmem_st32(ta, v);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            tc::tmem_st32(ta, o);
           }
         }
       }
-      // P row -> swizzled K-major bf16 tile (two 64-key halves)
+      // this half of the P row -> swizzled K-major bf16 tile
 #pragma unroll
-      for (int c16 = 0; c16 < KT / 8; ++c16) {
-        const int half = c16 >> 3, ch = c16 & 7;
-        const uint32_t addr = sP + half * HALF_B + r * 128 + ((ch ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(pk[4 * c16]),
-                     "r"(pk[4 * c16 + 1]), "r"(pk[4 * c16 + 2]), "r"(pk[4 * c16 + 3])
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const uint32_t addr = sP + ch * HALF_B + r * 128 + ((c8 ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(pk[4 * c8]),
+                     "r"(pk[4 * c8 + 1]), "r"(pk[4 * c8 + 2]), "r"(pk[4 * c8 + 3])
                      : "memory");
       }
       tc::fence_proxy_async_smem();
@@ -329,28 +350,35 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     }
     if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD), (nkt - 1) & 1, abort_flag, WAIT_LIMIT));
     if (ok) {
+      // full row sum from the two halves
+      float* xl = xch + 2 * 2 * 128;
+      xl[ch * 128 + r] = l;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(BAR(B_XL + quarter));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_XL + quarter), 0, abort_flag, WAIT_LIMIT));
+    }
+    if (ok) {
+      const float lt = l + xch[2 * 2 * 128 + (ch ^ 1) * 128 + r];
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const int head = w.kv_head * G + g;
       const int64_t row = (int64_t)(w.q_row + t);
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D +
+                                            ch * 64);
+      uint32_t o[64];
+      tc::tmem_ld64(tmem + lane_base + TMEM_O + col_half, o);
+      if (row_valid) {
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + lane_base + TMEM_O + c4 * 32, v);
-        if (row_valid) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack_bf16(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv);
-            u.y = pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv);
-            u.z = pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv);
-            u.w = pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
-            dst[c4 * 4 + q] = u;
-          }
+        for (int q = 0; q < 8; ++q) {
+          uint4 u;
+          u.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+          u.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          u.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+          u.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          dst[q] = u;
         }
+        if (ch == 0 && p.lse) p.lse[row * p.num_qo_heads + head] = (m_used + __log2f(lt)) * 0.69314718055994531f;
       }
-      if (row_valid && p.lse) p.lse[row * p.num_qo_heads + head] = (m_used + __log2f(l)) * 0.69314718055994531f;
     } else {
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
@@ -359,7 +387,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == MMA_WARP) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }
