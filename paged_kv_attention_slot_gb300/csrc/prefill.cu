@@ -153,11 +153,17 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     };
     bool ok = true;
     int pending = 0;  // tiles issued whose arrival is still owed
+    // slot rows of the next tile are loaded one iteration ahead so their latency overlaps the copies
+    int next_a = slot_of(w.kv_begin + pw * 64 + lane);
+    int next_b = slot_of(w.kv_begin + pw * 64 + 32 + lane);
     for (int j = 0; j < nkt && ok; ++j) {
       const int st = j & 1;
-      const int key0 = w.kv_begin + j * KT + pw * 64;
-      const int slot_a = slot_of(key0 + lane);
-      const int slot_b = slot_of(key0 + 32 + lane);
+      const int slot_a = next_a, slot_b = next_b;
+      if (j + 1 < nkt) {
+        const int key1 = w.kv_begin + (j + 1) * KT + pw * 64;
+        next_a = slot_of(key1 + lane);
+        next_b = slot_of(key1 + 32 + lane);
+      }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, WAIT_LIMIT));
       if (!ok) break;
       const uint32_t dst0 = s_base + st * TILE_B + half * HALF_B;
@@ -196,43 +202,55 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, true);
       bool ok = tc::mbar_wait(BAR(B_Q), 0, abort_flag, WAIT_LIMIT);
       tc::fence_after_sync();
-      for (int j = 0; j <= nkt && ok; ++j) {
-        if (j < nkt) {
-          const int st = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          ok = tc::mbar_wait(BAR(B_KF + st), ph, abort_flag, WAIT_LIMIT) &&
-               tc::mbar_wait(BAR(B_SE + st), ph ^ 1, abort_flag, WAIT_LIMIT);
-          if (!ok) break;
-          tc::fence_proxy_async_smem();
-          tc::fence_after_sync();
-          const uint32_t d = tmem + (uint32_t)st * KT;
+      // Issue S_j = Q K_j^T as soon as K_j has landed and its score buffer is free, and
+      // O += P_j V_j as soon as P_j and V_j are ready (in tile order each), polling both so
+      // neither waits behind the other's inputs.
+      int js = 0, jp = 0;  // next S tile, next PV tile
+      long long t0 = clock64();
+      while (ok && jp < nkt) {
+        bool progressed = false;
+        if (js < nkt && js <= jp + 1) {
+          const int st = js & 1;
+          const uint32_t ph = (js >> 1) & 1;
+          if (tc::mbar_try_wait(BAR(B_KF + st), ph) && tc::mbar_try_wait(BAR(B_SE + st), ph ^ 1)) {
+            tc::fence_proxy_async_smem();
+            tc::fence_after_sync();
+            const uint32_t d = tmem + (uint32_t)st * KT;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * HALF_B + (ks & 3) * 32;
-            const uint64_t a = tc::smem_desc_sw128(sQ + off, 16, 1024);
-            const uint64_t b = tc::smem_desc_sw128(sK + st * TILE_B + off, 16, 1024);
-            tc::mma_bf16_ss(d, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * HALF_B + (ks & 3) * 32;
+              const uint64_t a = tc::smem_desc_sw128(sQ + off, 16, 1024);
+              const uint64_t b = tc::smem_desc_sw128(sK + st * TILE_B + off, 16, 1024);
+              tc::mma_bf16_ss(d, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+            }
+            tc::commit(BAR(B_SF + st));
+            tc::commit(BAR(B_KE + st));
+            ++js;
+            progressed = true;
           }
-          tc::commit(BAR(B_SF + st));
-          tc::commit(BAR(B_KE + st));
         }
-        if (j >= 1) {
-          const int jp = j - 1;
+        if (jp < js) {
           const int st = jp & 1;
           const uint32_t ph = (jp >> 1) & 1;
-          ok = tc::mbar_wait(BAR(B_PF), jp & 1, abort_flag, WAIT_LIMIT) &&
-               tc::mbar_wait(BAR(B_VF + st), ph, abort_flag, WAIT_LIMIT);
-          if (!ok) break;
-          tc::fence_proxy_async_smem();
-          tc::fence_after_sync();
+          if (tc::mbar_try_wait(BAR(B_PF), jp & 1) && tc::mbar_try_wait(BAR(B_VF + st), ph)) {
+            tc::fence_proxy_async_smem();
+            tc::fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < KT / 16; ++kk) {
-            const uint64_t a = tc::smem_desc_sw128(sP + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
-            const uint64_t b = tc::smem_desc_sw128(sV + st * TILE_B + kk * 2048, HALF_B, 1024);
-            tc::mma_bf16_ss(tmem + TMEM_O, a, b, idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < KT / 16; ++kk) {
+              const uint64_t a = tc::smem_desc_sw128(sP + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
+              const uint64_t b = tc::smem_desc_sw128(sV + st * TILE_B + kk * 2048, HALF_B, 1024);
+              tc::mma_bf16_ss(tmem + TMEM_O, a, b, idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::commit(BAR(B_OD));
+            tc::commit(BAR(B_VE + st));
+            ++jp;
+            progressed = true;
           }
-          tc::commit(BAR(B_OD));
-          tc::commit(BAR(B_VE + st));
+        }
+        if (progressed) {
+          t0 = clock64();
+        } else if (*abort_flag || clock64() - t0 > WAIT_LIMIT) {
+          ok = false;
         }
       }
       if (!ok) {
