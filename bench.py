@@ -216,6 +216,32 @@ def cpu_baseline(b, pool, target_s=12.0):
 
 
 # ------------------------------------------------------------------------------------------------
+# multi-rank bookkeeping (one rank per GPU; each rank runs its own independent batch)
+# ------------------------------------------------------------------------------------------------
+def rank_batch(n: int, rank: int, scale_batch: float = 1.0):
+    """Rank `rank`'s batch of workload n: same shape, its own seed (weak scaling, no shared requests)."""
+    import workloads as W
+
+    return W.workload(n, seed_offset=rank, scale_batch=scale_batch)
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The slowest rank's time (all ranks must call it); identity without a process group."""
+    import torch
+
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the bytes every rank processed over the slowest rank's time."""
+    return bytes_per_rank_step * steps * world / (max_ms * 1e-3) / 1e9
+
+
+# ------------------------------------------------------------------------------------------------
 # the GPU arm
 # ------------------------------------------------------------------------------------------------
 def _device_state(b, device):
@@ -405,7 +431,7 @@ def main():
     pk._lib.lib()
     hbm, tf_burst, tf_sust, peak_src = _peaks()
 
-    b = W.workload(2, seed_offset=rank)
+    b = rank_batch(2, rank)
     st = _device_state(b, device)
     plan = pk.Plan()
     plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **_plan_kw(b))
@@ -415,12 +441,9 @@ def main():
     clocks.start()
     total_ms, run_ms = run_steps(b, st, plan, args.steps, args.warmup, dist_on)
     clk = clocks.stop()
-    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    if dist_on:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = max_over_ranks(total_ms, device)
     kv_bytes = b.kv_bytes_read()
-    value = kv_bytes * args.steps * world / (max_ms * 1e-3) / 1e9
+    value = aggregate_gbs(kv_bytes, args.steps, world, max_ms)
 
     e2e_dt, h2d, d2h = run_e2e(b, st, plan, max(3, args.steps // 2), 3)
     e2e_val = kv_bytes * max(3, args.steps // 2) / e2e_dt / 1e9
