@@ -219,6 +219,32 @@ int pkv_attn_decode_run(const pkv_plan* plan, const void* q, const pkv_cache* ca
 int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
                          void* stream);
 
+/*
+ * pkv_attn_decode_run_noalloc: pkv_attn_decode_run for callers that cannot allocate device memory.
+ * (The pages have no counterpart: this entry point is an addition of this library.)
+ *
+ * Who needs it: code that is not allowed to call cudaMalloc -- a host framework whose memory pool
+ * forbids raw allocations, a caller in the middle of building a CUDA graph, or an embedded runtime
+ * that receives a fixed device-memory budget up front -- and therefore cannot provide the plan
+ * workspace.  This call needs no workspace: the plan's metadata (work list, per-request facts,
+ * page list) and the split-KV partial outputs live in one statically sized device array inside the
+ * library (32 MiB per device that loads the library, held until the process exits).  The caller
+ * still passes Q, the cache and the outputs, exactly as for pkv_attn_decode_run.
+ *
+ *   plan   a PKV_MODE_DECODE plan; a host-only plan (pkv_attn_plan with workspace == NULL) is
+ *          enough, and its workspace, if any, is not used.  Its pkv_plan_info().workspace_bytes
+ *          must not exceed 32 MiB, otherwise PKV_EWORKSPACE is returned and nothing runs.
+ * Same kernels, outputs and error checks as pkv_attn_decode_run.  The call itself allocates no
+ * device or pinned memory: it copies the plan's metadata from its host arrays into the static
+ * array on `stream`, then launches the kernels.
+ * Every call shares the one array per device and it keeps the last call's contents; calls whose
+ * work may overlap on the GPU (other streams, other threads) race on it and must be serialised by
+ * the caller.  The first call on a device looks up the array's device address; make that first
+ * call before any stream capture begins.
+ */
+int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                                void* stream);
+
 /* ---------------------------------------------------------------------------------------------- */
 /* errors and inspection                                                                          */
 /* ---------------------------------------------------------------------------------------------- */

@@ -100,6 +100,7 @@ _SIGS = {
     "pkv_plan_workspace_size": (C.c_int, [C.POINTER(pkv_plan_args), C.POINTER(C.c_size_t)]),
     "pkv_attn_plan": (C.c_int, [C.c_void_p, C.POINTER(pkv_plan_args), C.c_void_p, C.c_size_t, C.c_void_p]),
     "pkv_attn_decode_run": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
+    "pkv_attn_decode_run_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_attn_prefill_run": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_last_error": (C.c_char_p, []),
     "pkv_device_error": (C.c_int, [_i32p, C.c_int32, C.c_void_p]),

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "pkv_attn.h"
 
 namespace pkv {
@@ -84,4 +86,29 @@ int prefill_supported(const char** why);
 
 cudaError_t read_device_error(int32_t* code, int reset, cudaStream_t s);
 
+// record `msg` as this thread's pkv_last_error() text and return `code`
+int set_last_error(int code, const char* msg);
+
 }  // namespace pkv
+
+// Host-side plan object behind the opaque pkv_plan handle.
+struct pkv_plan {
+  bool valid = false;
+  int32_t mode = 0, batch = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, window_left = -1, kv_dtype = 0, q_dtype = 0;
+  float sm_scale = 0.f;
+  int64_t total_tokens = 0, max_page_id = -1, kv_tokens = 0, kv_chunk = 0, num_partials = 0;
+  std::vector<pkv::WorkItem> work;
+  std::vector<pkv::MergeItem> merge;
+  std::vector<pkv::ReqInfo> req;
+  std::vector<int32_t> indices;
+  size_t off_work = 0, off_merge = 0, off_req = 0, off_idx = 0, off_plse = 0, off_po = 0;
+  size_t meta_bytes = 0, need_bytes = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  void* pinned = nullptr;
+  size_t pinned_bytes = 0;
+  cudaEvent_t copy_done = nullptr;
+  bool copy_pending = false;
+  int device = -1;
+};
+
