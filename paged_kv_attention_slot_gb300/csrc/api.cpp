@@ -189,6 +189,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   P->total_tokens = total_tokens;
   P->work.clear();
   P->merge.clear();
+  P->slot_unit.clear();
   P->num_partials = 0;
   P->kv_tokens = 0;
   P->kv_chunk = 0;
@@ -270,6 +271,9 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
       }
     }
     P->num_partials = slot;
+    P->slot_unit.resize((size_t)slot);
+    for (size_t u = 0; u < P->merge.size(); ++u)
+      for (int32_t k = 0; k < P->merge[u].num_splits; ++k) P->slot_unit[P->merge[u].first_slot + k] = (int32_t)u;
   } else {
     const int32_t tok_per_tile = kPrefillRows / G;
     for (int32_t i = 0; i < B; ++i) {
@@ -309,6 +313,10 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   off = align_up(off + P->req.size() * sizeof(ReqInfo), 256);
   P->off_idx = off;
   off = align_up(off + P->indices.size() * sizeof(int32_t), 256);
+  P->off_slot_unit = off;
+  off = align_up(off + P->slot_unit.size() * sizeof(int32_t), 256);
+  P->off_count = off;  // zero-filled by the metadata copy; the kernel leaves it zero after each run
+  off = align_up(off + P->merge.size() * sizeof(int32_t), 256);
   P->meta_bytes = off;
   P->off_plse = off;
   off = align_up(off + (size_t)P->num_partials * pkv::kDecodeRows * sizeof(float), 256);
@@ -350,6 +358,8 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
   p.kv_indices = (const int32_t*)(ws + P->off_idx);
   p.part_lse = (float*)(ws + P->off_plse);
   p.part_o = (float*)(ws + P->off_po);
+  p.slot_unit = (const int32_t*)(ws + P->off_slot_unit);
+  p.unit_count = (int32_t*)(ws + P->off_count);
   p.q = q;
   p.o = o;
   p.lse = lse;
@@ -490,6 +500,7 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
   std::memcpy(h + plan->off_merge, plan->merge.data(), plan->merge.size() * sizeof(MergeItem));
   std::memcpy(h + plan->off_req, plan->req.data(), plan->req.size() * sizeof(ReqInfo));
   std::memcpy(h + plan->off_idx, plan->indices.data(), plan->indices.size() * sizeof(int32_t));
+  std::memcpy(h + plan->off_slot_unit, plan->slot_unit.data(), plan->slot_unit.size() * sizeof(int32_t));
   cudaStream_t s = (cudaStream_t)stream;
   PKV_CUDA(cudaMemcpyAsync(workspace, h, plan->meta_bytes, cudaMemcpyHostToDevice, s), "plan metadata copy");
   PKV_CUDA(cudaEventRecord(plan->copy_done, s), "cudaEventRecord");
@@ -536,7 +547,6 @@ int pkv_attn_decode_run(const pkv_plan* plan, const void* q, const pkv_cache* ca
   if (plan->work.empty()) return PKV_OK;
   pkv::RunParams p = make_params(plan, q, cache, o, lse);
   PKV_CUDA(pkv::launch_decode(p, cache->dtype, (cudaStream_t)stream), "decode launch");
-  if (!plan->merge.empty()) PKV_CUDA(pkv::launch_merge(p, (cudaStream_t)stream), "merge launch");
   return PKV_OK;
 }
 

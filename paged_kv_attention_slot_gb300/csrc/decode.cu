@@ -1,4 +1,4 @@
-// Batched paged decode (one new token per request) and the split-KV merge.
+// Batched paged decode (one new token per request) with the split-KV merge fused in.
 //
 // What it computes: for request i, KV head h and every query head of h's group, the softmax over
 // the visible keys of the scaled scores q.k_j, applied to v_j, with K/V read through the CSR page
@@ -23,8 +23,9 @@
 //    is permuted identically for Q and K (a sum does not depend on order) so that one ldmatrix feeds
 //    two code bytes per register half directly;
 //  * the 4 warps merge their softmax states through shared memory at the end; a CTA either writes
-//    the final bf16 output (no split) or a normalised fp32 partial plus its log2-sum-exp, which the
-//    merge kernel combines: m = max lse_s, o = sum_s 2^(lse_s - m) o_s / sum_s 2^(lse_s - m).
+//    the final bf16 output (no split) or a normalised fp32 partial plus its log2-sum-exp; the last
+//    CTA of a split unit to finish (an atomic count per unit, reset after use, no waiting) merges
+//    the unit: m = max lse_s, o = sum_s 2^(lse_s - m) o_s / sum_s 2^(lse_s - m).
 
 #include <cuda_bf16.h>
 #include <math.h>
@@ -123,13 +124,20 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
   constexpr int RPI = 32 / C::CH;  // rows per warp instruction
   const int lc = lane % C::CH;
   const int lsub = lane / C::CH;
+  // The page id of the row this lane resolves is fetched one tile ahead (this warp's next tile is
+  // 4 tiles = 64 keys further), so the index load never stalls the issue of the copies.
+  auto fetch_page = [&](int key) -> int {
+    return key < w.kv_end ? __ldg(p.kv_indices + ri.page_base + key / p.page_size) : 0;
+  };
+  int next_page = fetch_page(w.kv_begin + warp * C::KEYS + lr);
   auto load_tile = [&](int i, int stage) {
     const int key = w.kv_begin + (warp + i * C::WARPS) * C::KEYS + lr;
+    const int page = next_page;
+    next_page = fetch_page(key + C::WARPS * C::KEYS);
     int64_t roff = -1;
     if (key < w.kv_end) {
       const int lp = key / p.page_size;
       const int off = key - lp * p.page_size;
-      const int page = __ldg(p.kv_indices + ri.page_base + lp);
       if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages)
         record_error(err, PKV_DEVERR_PAGE_RANGE);
       else
@@ -351,37 +359,44 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
       po[idx] = acc;
     }
     if (threadIdx.x < rows) p.part_lse[(int64_t)w.out_slot * kDecodeRows + threadIdx.x] = s_lse2[threadIdx.x];
-  }
-}
-
-// Split-KV reduction: one CTA per (request, KV head, head group) with more than one chunk.
-template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const RunParams p) {
-  const MergeItem m = p.merge[blockIdx.x];
-  const int qh0 = m.kv_head * p.group + m.head_group * kDecodeRows;
-  const int rows = min(kDecodeRows, p.group - m.head_group * kDecodeRows);
-  __shared__ float sM[kDecodeRows], sInv[kDecodeRows];
-  const float* lse = p.part_lse + (int64_t)m.first_slot * kDecodeRows;
-  if (threadIdx.x < rows) {
-    const int r = threadIdx.x;
-    float M = -INFINITY;
-    for (int s = 0; s < m.num_splits; ++s) M = fmaxf(M, lse[s * kDecodeRows + r]);
-    float W = 0.f;
-    for (int s = 0; s < m.num_splits; ++s) W += ex2(lse[s * kDecodeRows + r] - M);
-    sM[r] = M;
-    sInv[r] = 1.f / W;
-    if (p.lse) p.lse[(int64_t)m.q_row * p.num_qo_heads + qh0 + r] = (M + __log2f(W)) * 0.69314718055994531f;
-  }
-  __syncthreads();
-  const float* po = p.part_o + (int64_t)m.first_slot * kDecodeRows * D;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((int64_t)m.q_row * p.num_qo_heads + qh0) * D;
-  for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
-    const int r = idx / D;
-    const float M = sM[r];
-    float acc = 0.f;
-    for (int s = 0; s < m.num_splits; ++s)
-      acc += ex2(lse[s * kDecodeRows + r] - M) * po[(int64_t)s * kDecodeRows * D + idx];
-    out[idx] = __float2bfloat16_rn(acc * sInv[r] * p.out_scale);
+    // The last chunk of a (request, KV head, group) to finish merges all of its partials:
+    // m = max lse_s, o = sum_s 2^(lse_s - m) o_s / sum_s 2^(lse_s - m).  No CTA waits for another.
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    const int unit = p.slot_unit[w.out_slot];
+    const MergeItem m = p.merge[unit];
+    if (threadIdx.x == 0) {
+      const int done = atomicAdd(p.unit_count + unit, 1);
+      s_last = done == m.num_splits - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    __shared__ float sM[kDecodeRows], sInv[kDecodeRows];
+    const float* lse = p.part_lse + (int64_t)m.first_slot * kDecodeRows;
+    if (threadIdx.x < rows) {
+      const int r = threadIdx.x;
+      float M = -INFINITY;
+      for (int s = 0; s < m.num_splits; ++s) M = fmaxf(M, __ldcg(lse + s * kDecodeRows + r));
+      float W = 0.f;
+      for (int s = 0; s < m.num_splits; ++s) W += ex2(__ldcg(lse + s * kDecodeRows + r) - M);
+      sM[r] = M;
+      sInv[r] = 1.f / W;
+      if (p.lse) p.lse[(int64_t)m.q_row * p.num_qo_heads + qh0 + r] = (M + __log2f(W)) * 0.69314718055994531f;
+    }
+    __syncthreads();
+    const float* pm = p.part_o + (int64_t)m.first_slot * kDecodeRows * D;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((int64_t)m.q_row * p.num_qo_heads + qh0) * D;
+    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
+      const int r = idx / D;
+      const float M = sM[r];
+      float acc = 0.f;
+      for (int s = 0; s < m.num_splits; ++s)
+        acc += ex2(__ldcg(lse + s * kDecodeRows + r) - M) * __ldcg(pm + (int64_t)s * kDecodeRows * D + idx);
+      out[idx] = __float2bfloat16_rn(acc * sInv[r] * p.out_scale);
+    }
+    if (threadIdx.x == 0) p.unit_count[unit] = 0;  // ready for the next run of this plan
   }
 }
 
@@ -410,15 +425,6 @@ cudaError_t launch_decode(const RunParams& p, int kv_dtype, cudaStream_t s) {
   if (p.head_dim == 128) return launch_decode_t<128, false>(p, s);
   if (p.head_dim == 64) return launch_decode_t<64, false>(p, s);
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_merge(const RunParams& p, cudaStream_t s) {
-  if (p.num_merge <= 0) return cudaSuccess;
-  if (p.head_dim == 128)
-    merge_kernel<128><<<(unsigned)p.num_merge, 128, 0, s>>>(p);
-  else
-    merge_kernel<64><<<(unsigned)p.num_merge, 128, 0, s>>>(p);
-  return cudaGetLastError();
 }
 
 }  // namespace pkv

@@ -6,11 +6,12 @@
 // memory up front.  For them, pkv_attn_decode_run_noalloc keeps everything the decode needs
 // besides its inputs and outputs -- the plan's work list, the per-request facts, the page list and
 // the split-KV partial outputs -- in one file-scope __device__ array of kNoAllocScratchBytes, and
-// runs the same decode and merge kernels as pkv_attn_decode_run on it.
+// runs the same decode kernel (with its split-KV merge) as pkv_attn_decode_run on it.
 //
 // The array exists once per device that loads the library and stays allocated until the process
 // exits.  Every call shares it and it keeps the last call's contents; nothing in it has to start at
-// zero (every partial slot a call reads was written earlier in the same call).  Two calls whose
+// zero except the per-unit split counters, which every call clears before its kernels run (every
+// partial slot a call reads was written earlier in the same call).  Two calls whose
 // work overlaps on the GPU (different streams, or different host threads without ordering) race
 // on the array.  The first call on a device looks up the array's device address; that first call
 // should be made before any stream capture begins.
@@ -91,16 +92,21 @@ extern "C" int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, 
   char* base = static_cast<char*>(ws);
   // the plan's metadata, straight from its host arrays (stream-ordered before the kernels)
   struct Seg { size_t off; const void* src; size_t bytes; };
-  const Seg segs[4] = {
+  const Seg segs[5] = {
       {plan->off_work, plan->work.data(), plan->work.size() * sizeof(WorkItem)},
       {plan->off_merge, plan->merge.data(), plan->merge.size() * sizeof(MergeItem)},
       {plan->off_req, plan->req.data(), plan->req.size() * sizeof(ReqInfo)},
       {plan->off_idx, plan->indices.data(), plan->indices.size() * sizeof(int32_t)},
+      {plan->off_slot_unit, plan->slot_unit.data(), plan->slot_unit.size() * sizeof(int32_t)},
   };
   for (const Seg& g : segs) {
     if (!g.bytes) continue;
     e = cudaMemcpyAsync(base + g.off, g.src, g.bytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return noalloc_fail(PKV_ECUDA, std::string("metadata copy: ") + cudaGetErrorString(e));
+  }
+  if (!plan->merge.empty()) {
+    e = cudaMemsetAsync(base + plan->off_count, 0, plan->merge.size() * sizeof(int32_t), s);
+    if (e != cudaSuccess) return noalloc_fail(PKV_ECUDA, std::string("counter reset: ") + cudaGetErrorString(e));
   }
 
   RunParams p{};
@@ -110,6 +116,8 @@ extern "C" int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, 
   p.kv_indices = reinterpret_cast<const int32_t*>(base + plan->off_idx);
   p.part_lse = reinterpret_cast<float*>(base + plan->off_plse);
   p.part_o = reinterpret_cast<float*>(base + plan->off_po);
+  p.slot_unit = reinterpret_cast<const int32_t*>(base + plan->off_slot_unit);
+  p.unit_count = reinterpret_cast<int32_t*>(base + plan->off_count);
   p.q = q;
   p.o = o;
   p.lse = lse;
@@ -131,9 +139,5 @@ extern "C" int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, 
   p.num_merge = (int64_t)plan->merge.size();
   e = launch_decode(p, cache->dtype, s);
   if (e != cudaSuccess) return noalloc_fail(PKV_ECUDA, std::string("decode launch: ") + cudaGetErrorString(e));
-  if (p.num_merge > 0) {
-    e = launch_merge(p, s);
-    if (e != cudaSuccess) return noalloc_fail(PKV_ECUDA, std::string("merge launch: ") + cudaGetErrorString(e));
-  }
   return PKV_OK;
 }

@@ -54,6 +54,8 @@ struct RunParams {
   const int32_t* kv_indices;
   float* part_o;    // [num_partials, 16, head_dim]
   float* part_lse;  // [num_partials, 16] (log2 units)
+  const int32_t* slot_unit;  // [num_partials]: merge item of each partial slot
+  int32_t* unit_count;       // [num_merge]: partials written so far (0 between runs)
   const void* q;
   void* o;
   float* lse;  // nullable
@@ -79,7 +81,6 @@ struct RunParams {
 cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, int64_t T, const pkv_cache& c,
                             float inv_k, float inv_v, cudaStream_t s);
 cudaError_t launch_decode(const RunParams& p, int kv_dtype, cudaStream_t s);
-cudaError_t launch_merge(const RunParams& p, cudaStream_t s);
 cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v,
                            int64_t total_tokens, cudaStream_t s);
 int prefill_supported(const char** why);
@@ -101,7 +102,9 @@ struct pkv_plan {
   std::vector<pkv::MergeItem> merge;
   std::vector<pkv::ReqInfo> req;
   std::vector<int32_t> indices;
-  size_t off_work = 0, off_merge = 0, off_req = 0, off_idx = 0, off_plse = 0, off_po = 0;
+  size_t off_work = 0, off_merge = 0, off_req = 0, off_idx = 0, off_slot_unit = 0, off_count = 0, off_plse = 0,
+         off_po = 0;
+  std::vector<int32_t> slot_unit;
   size_t meta_bytes = 0, need_bytes = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
