@@ -451,7 +451,7 @@ def main():
 
     run_avg = statistics.mean(run_ms)
     achieved = kv_bytes / (run_avg * 1e-3) / 1e9
-    launches_per_step = 2 + (1 if info["num_merge"] > 0 else 0)
+    launches_per_step = 2  # kv_store + decode (the split-KV merge runs inside the decode kernel)
 
     prefill = None
     if not args.no_prefill and rank == 0:
@@ -487,7 +487,7 @@ def main():
             },
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src,
-                         "kernel": "decode_run (decode + split-KV merge kernels)",
+                         "kernel": "decode_kernel (split-KV merge fused), one launch per decode_run",
                          "traffic": _traffic("decode", ["decode.cu", "ptx.cuh"])},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,

@@ -48,7 +48,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Decode kernel occupancy assumed by the split policy (it is launched with 2 CTAs per SM).
 constexpr int kDecodeCtasPerSm = 2;
-constexpr int kDecodeWaves = 4;          // target CTAs = SMs * CTAs/SM * waves
+constexpr int kDecodeWaves = 1;          // chunk = total work / (SMs * CTAs/SM * waves)
 constexpr int kDecodeMinChunk = 256;     // never split below this many keys
 constexpr int kDecodeChunkAlign = 64;    // 4 warps x 16 keys
 constexpr int kPrefillRows = 128;        // query rows (tokens x heads of one KV head) per CTA
@@ -221,10 +221,16 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     }
     P->kv_chunk = chunk;
     // exact CTA count first, then fill in place
+    // A unit is split only when it is clearly longer than the chunk: every split costs a partial
+    // write and a merge, and units up to 1.25 chunks still balance under longest-first launch.
+    auto num_splits = [&](int64_t len) -> int64_t {
+      if (len <= chunk + chunk / 4) return 1;
+      return (len + chunk - 1) / chunk;
+    };
     int64_t items = 0, merges = 0;
     for (const Unit& u : units) {
       const int64_t len = u.hi - u.lo;
-      int64_t ns = (len + chunk - 1) / chunk;
+      int64_t ns = num_splits(len);
       if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
       const int64_t c = align_up((len + ns - 1) / ns, 16);
       ns = (len + c - 1) / c;
@@ -239,7 +245,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     int64_t slot = 0;
     for (const Unit& u : units) {
       const int64_t len = u.hi - u.lo;
-      int64_t ns = (len + chunk - 1) / chunk;
+      int64_t ns = num_splits(len);
       if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
       const int64_t c = align_up((len + ns - 1) / ns, 16);
       ns = (len + c - 1) / c;
