@@ -142,7 +142,7 @@ def test_decode_gqa_groups(hq, hkv):
 def test_decode_split_kv_merge(max_splits):
     lens = [3000, 9000, 64, 4500, 12000, 1]
     b = W.make_batch(lens, [1] * len(lens), 16, 32, 8, 128, seed=77)
-    stats, plan = _decode_case(b, max_splits=max_splits, num_sms=8)  # few SMs -> many splits
+    stats, plan = _decode_case(b, max_splits=max_splits, num_sms=64)  # small chunks -> many splits
     info = plan.info()
     if max_splits == 1:
         assert info["num_merge"] == 0
@@ -154,7 +154,7 @@ def test_decode_split_kv_merge(max_splits):
 def test_decode_sliding_window(window):
     lens = [1, 50, 4097, 6000, 9000]
     b = W.make_batch(lens, [1] * len(lens), 32, 16, 4, 128, seed=window + 3, window_left=window)
-    _decode_case(b, num_sms=16)
+    _decode_case(b, num_sms=64)
 
 
 def test_decode_idle_requests_and_custom_scale():
@@ -166,7 +166,7 @@ def test_decode_idle_requests_and_custom_scale():
 def test_decode_fp8_small_with_window():
     for w in (-1, 700):
         b = W.make_batch([5000, 131, 2048, 1], [1] * 4, 128, 32, 8, 128, seed=55, kv_dtype="e4m3", window_left=w)
-        _decode_case(b, num_sms=24)
+        _decode_case(b, num_sms=64)
 
 
 def test_decode_plan_reuse_across_layers_and_replan():

@@ -50,10 +50,10 @@ def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
     refs = []
     for b, g in zip(batches, gpu):
         g.store()
-        ref_plan = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **_plan_kw(b, num_sms=8))
+        ref_plan = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **_plan_kw(b, num_sms=64))
         refs.append(g.run(ref_plan))
     host_plans = [pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len,
-                                 **_plan_kw(b, num_sms=8), host_only=True) for b in batches]
+                                 **_plan_kw(b, num_sms=64), host_only=True) for b in batches]
     assert host_plans[0].info()["num_merge"] > 0
 
     tol = {"bf16": G.BF16_MAX_ABS, "e4m3": G.FP8_MAX_ABS}
