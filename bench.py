@@ -148,6 +148,10 @@ def _oracle_worker_init(workload_n, seed_offset):
     _WORKER_BATCH = (b, bits(b.q), bits(b.k_pool), bits(b.v_pool))
 
 
+def _noop(_):
+    return _WORKER_BATCH is not None
+
+
 def _oracle_request_task(i):
     """Worker: the oracle, as it stands, on request i of the batch (its one query token)."""
     import numpy as np
@@ -178,6 +182,11 @@ class OraclePool:
                     os.environ.pop(k, None)
                 else:
                     os.environ[k] = v
+
+    def wait_ready(self):
+        """Block until every worker has finished its (CPU-heavy) initialisation, so no worker competes
+        with the GPU timing for host cores."""
+        self.pool.map(_noop, range(4 * self.cores), chunksize=1)
 
     def run(self, b, req_ids):
         """Wall time of the oracle over these requests, one request per task."""
@@ -422,6 +431,8 @@ def main():
 
     # the oracle pool is spawned before the first GPU call
     pool = OraclePool(2, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if pool is not None:
+        pool.wait_ready()
 
     dist_on = world > 1
     if dist_on:
@@ -508,6 +519,7 @@ def reference_arm(args, world, rank):
     import workloads as W
 
     pool = OraclePool(2, 0)
+    pool.wait_ready()
     b = W.workload(2)
     ids = list(range(b.batch_size))
     per_step = ids[:8]  # bounded sample per step: 8 of the 64 requests
