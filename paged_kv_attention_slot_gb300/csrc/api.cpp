@@ -51,7 +51,8 @@ constexpr int kDecodeCtasPerSm = 2;
 constexpr int kDecodeWaves = 1;          // chunk = total work / (SMs * CTAs/SM * waves)
 constexpr int kDecodeMinChunk = 256;     // never split below this many keys
 constexpr int kDecodeChunkAlign = 64;    // 4 warps x 16 keys
-constexpr int kPrefillRows = 128;        // query rows (tokens x heads of one KV head) per CTA
+constexpr int kPrefillRows = 128;        // query rows (tokens x heads of one KV head) per Q tile
+constexpr int kPrefillTiles = 2;         // Q tiles per CTA (they share every K/V tile)
 
 }  // namespace
 
@@ -281,7 +282,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     for (size_t u = 0; u < P->merge.size(); ++u)
       for (int32_t k = 0; k < P->merge[u].num_splits; ++k) P->slot_unit[P->merge[u].first_slot + k] = (int32_t)u;
   } else {
-    const int32_t tok_per_tile = kPrefillRows / G;
+    const int32_t tok_per_tile = kPrefillTiles * (kPrefillRows / G);  // tokens per CTA
     for (int32_t i = 0; i < B; ++i) {
       const ReqInfo& r = P->req[i];
       for (int32_t t0 = 0; t0 < r.q_len; t0 += tok_per_tile) {

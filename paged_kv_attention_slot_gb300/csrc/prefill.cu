@@ -8,28 +8,29 @@
 // Builder 的结果»: multi-token queries apply the causal mask inside their own request only;
 // "手写 mini-sglang 阶段四 · GPU 注意力后端", section «在 CPU 上验证»: queries are the last n positions).
 //
-// GB300 design (one CTA = 128 query rows x one KV head; rows are (token, head) pairs of the KV
-// head's query-head group, so every K/V tile feeds all G heads):
-//  * warps 9-12 (producers): the Q tile by one 3-D TMA box; K (warps 9-10) and V (warps 11-12) tiles of
-//    128 keys gathered row by row through the page table with 16-byte cp.async, 16 lanes per
-//    256-byte row (fully coalesced), written straight into the 128-byte-swizzled K-major layout
-//    the tensor core reads, double-buffered; each producer thread waits for its own copies, fences
-//    them into the async proxy and arrives on the stage's mbarrier.  (TMA tile::gather4 moves only
-//    512 bytes per instruction; issued one lane at a time it was the bottleneck for token-granular
-//    pools, which is why the rows go through cp.async instead);
-//  * warp 8 (MMA): one elected thread issues tcgen05.mma (M=128, N=128, K=16, bf16 in, fp32 out):
-//    S_j = Q K_j^T into one of two TMEM score buffers, and O += P_{j-1} V_{j-1} into a TMEM output
-//    accumulator, software-pipelined so S_j runs while the softmax works on tile j-1;
-//  * warps 0-7 (softmax): warp w owns query rows 32 (w % 4) .. +31 (= its TMEM lanes) and key
-//    columns 64 (w / 4) .. +63 of every tile: one tcgen05.ld of its 64 scores, causal/window mask on
-//    diagonal tiles only, row maximum shared with the partner warp of the other column half through
-//    shared memory and a 2-arrival mbarrier (bounded wait), online softmax in base 2 with the score scale
-//    folded into one FFMA before ex2, and a lazy rescale (the reference maximum only moves when a
-//    row's maximum grows by more than 2^8, exact because numerator and denominator share the
-//    reference); P written as bf16 into a swizzled shared tile for the next MMA, O rescaled in TMEM
-//    only when needed, then the final O / l and log-sum-exp.
-// Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its
-// own copies and MMAs, frees its TMEM and exits.
+// GB300 design.  One CTA = two 128-row query tiles (A and B: consecutive tokens of one request, rows
+// = (token, head) pairs of one KV head's query-head group) sharing every K/V tile, so each gathered
+// K/V byte feeds twice the tensor-core work of a single tile:
+//  * warps 9-12 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps 9-10) and V
+//    (warps 11-12) tiles of 128 keys gathered row by row through the page table with 16-byte
+//    cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the tensor core
+//    reads; two stages; each producer thread waits for its own copies, fences them into the async
+//    proxy and arrives on the stage's mbarrier.  (TMA tile::gather4 moves 512 bytes per instruction
+//    and measured slower here for token-granular pools.)
+//  * warp 8 (MMA): one thread issues tcgen05.mma (kind::f16, M=128, N=128, K=16, bf16 in, fp32
+//    accumulate in TMEM) in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ..., so the
+//    tensor core works on one tile while the other tile's softmax runs.  P lives in TMEM on top of
+//    its own scores and is the A operand of the PV MMA (V is an MN-major shared-memory operand, no
+//    transpose).  MMAs of one thread execute in issue order, so S_X(j+1) overwriting P_X(j) is safe
+//    once PV_X(j) was issued, and "S_X(j) complete" implies "PV_X(j-1) complete".
+//  * warps 0-3 / 4-7 (softmax of tile A / B): thread r owns row r (TMEM lane r).  Pass 1 reads the
+//    128 scores in 32-column loads for the row maximum; pass 2 re-reads them, computes
+//    p = 2^(s * scale * log2 e - m) with one FFMA + ex2, packs bf16 pairs and stores them over the
+//    scores already consumed.  Causal / window masking only on tiles that need it.  The row maximum
+//    moves lazily (only when it grows by more than 2^8; exact because numerator and denominator
+//    share it), and O is rescaled in TMEM only then.  Epilogue: O / l to bf16 rows and the LSE.
+// Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its own
+// copies and MMAs, frees its TMEM and exits.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,32 +45,32 @@ namespace pkv {
 int32_t* device_error_ptr();
 
 namespace pf {
-constexpr int ROWS = 128;               // query rows per CTA
+constexpr int ROWS = 128;               // query rows per Q tile
 constexpr int KT = 128;                 // keys per K/V tile
 constexpr int D = 128;                  // head dim
 constexpr int HALF_B = ROWS * 128;      // one 64-column half of a 128-row bf16 tile (16 KB)
 constexpr int TILE_B = 2 * HALF_B;      // 32 KB
 constexpr int STAGES = 2;
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE_B;
+constexpr int OFF_QA = 0;
+constexpr int OFF_QB = OFF_QA + TILE_B;
+constexpr int OFF_K = OFF_QB + TILE_B;
 constexpr int OFF_V = OFF_K + STAGES * TILE_B;
-constexpr int OFF_P = OFF_V + STAGES * TILE_B;
-constexpr int OFF_BAR = OFF_P + TILE_B;
-constexpr int NUM_BARS = 32;
+constexpr int OFF_BAR = OFF_V + STAGES * TILE_B;
+constexpr int NUM_BARS = 16;
 constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
-constexpr int OFF_XCH = OFF_ABORT + 8;               // row-max exchange [2 tiles][2 halves][128] + sums
-constexpr int SMEM_USED = OFF_XCH + (2 * 2 * 128 + 2 * 128) * 4;
+constexpr int SMEM_USED = OFF_ABORT + 8;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024 bytes
 enum {
-  B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7, B_SF = 9, B_SE = 11, B_PF = 13, B_OD = 14, B_FIN = 15,
-  B_XM = 16,  // [4 row quarters][2 tile parities]: the two column-half warps exchanged their maxima
-  B_XL = 24   // [4 row quarters]: the two column-half warps exchanged their final row sums
+  B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7,
+  B_SF = 9,   // [2]: S_X(j) complete (and with it PV_X(j-1))
+  B_PF = 11,  // [2]: P_X(j) stored in TMEM by the 4 softmax warps of tile X
+  B_OD = 13,  // [2]: the last PV_X complete
+  B_FIN = 15
 };
-constexpr uint32_t TMEM_COLS = 512;     // S0 [0,128), S1 [128,256), O [256,384)
+constexpr uint32_t TMEM_COLS = 512;  // S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384), O_B [384,512)
 constexpr uint32_t TMEM_O = 256;
-constexpr int THREADS = 416;  // 8 softmax warps, 1 MMA warp, 2 K-producer warps, 2 V-producer warps
-constexpr int SOFTMAX_WARPS = 8;
+constexpr int THREADS = 416;          // 8 softmax warps, 1 MMA warp, 4 producer warps
 constexpr int MMA_WARP = 8;
 constexpr int PRODUCER_WARP0 = 9;
 constexpr int PRODUCER_THREADS = 64;  // per operand (K or V)
@@ -77,7 +78,7 @@ constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 }  // namespace pf
 
-__global__ void __launch_bounds__(pf::THREADS, 1)
+__global__ void __maxnreg__(152)
     prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, int32_t* err) {
   using namespace pf;
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base = (raw_u + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw_u);
-  const uint32_t sQ = base + OFF_Q, sK = base + OFF_K, sV = base + OFF_V, sP = base + OFF_P;
+  const uint32_t sQ = base + OFF_QA, sK = base + OFF_K, sV = base + OFF_V;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + OFF_ABORT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + OFF_TMEM);
 #define BAR(i) (base + OFF_BAR + 8u * (uint32_t)(i))
@@ -95,7 +96,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const WorkItem w = p.work[blockIdx.x];
   const ReqInfo ri = p.req[w.req];
   const int G = p.group;
+  const int T = ROWS / G;              // tokens per Q tile
+  const bool two = w.q_rows > T;       // does tile B hold any token?
   const int nkt = (w.kv_end - w.kv_begin + KT - 1) / KT;
+  (void)tk;
+  (void)tv;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -105,14 +110,13 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       tc::mbar_init(BAR(B_VF + s), PRODUCER_THREADS);
       tc::mbar_init(BAR(B_KE + s), 1);
       tc::mbar_init(BAR(B_VE + s), 1);
-      tc::mbar_init(BAR(B_SF + s), 1);
-      tc::mbar_init(BAR(B_SE + s), SOFTMAX_WARPS);
     }
-    tc::mbar_init(BAR(B_PF), SOFTMAX_WARPS);
-    tc::mbar_init(BAR(B_OD), 1);
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(BAR(B_SF + x), 1);
+      tc::mbar_init(BAR(B_PF + x), 4);
+      tc::mbar_init(BAR(B_OD + x), 1);
+    }
     tc::mbar_init(BAR(B_FIN), 1);
-    for (int i = 0; i < 8; ++i) tc::mbar_init(BAR(B_XM + i), 2);
-    for (int i = 0; i < 4; ++i) tc::mbar_init(BAR(B_XL + i), 2);
     tc::mbar_fence_init();
   }
   if (warp == MMA_WARP) {
@@ -127,16 +131,20 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   if (warp >= PRODUCER_WARP0) {
     // ------------------------------------------------------------------ producers (cp.async)
     const bool is_k = warp < PRODUCER_WARP0 + 2;
-    const int pw = (warp - PRODUCER_WARP0) & 1;  // which 64-row half of the tile this warp fills
+    const int pw = (warp - PRODUCER_WARP0) & 1;  // which 64-row half of the K/V tile this warp fills
     const char* pool = is_k ? p.k_pool : p.v_pool;
     const uint32_t s_base = is_k ? sK : sV;
     const uint32_t full0 = is_k ? BAR(B_KF) : BAR(B_VF);
     const uint32_t empty0 = is_k ? BAR(B_KE) : BAR(B_VE);
     if (warp == PRODUCER_WARP0 && lane == 0) {
       tc::tma_prefetch_desc(&tq);
-      tc::mbar_arrive_expect_tx(BAR(B_Q), TILE_B);
+      tc::mbar_arrive_expect_tx(BAR(B_Q), two ? 2 * TILE_B : TILE_B);
       tc::tma_load_3d(sQ, &tq, BAR(B_Q), 0, w.kv_head * G, w.q_row);
       tc::tma_load_3d(sQ + HALF_B, &tq, BAR(B_Q), 64, w.kv_head * G, w.q_row);
+      if (two) {
+        tc::tma_load_3d(sQ + TILE_B, &tq, BAR(B_Q), 0, w.kv_head * G, w.q_row + T);
+        tc::tma_load_3d(sQ + TILE_B + HALF_B, &tq, BAR(B_Q), 64, w.kv_head * G, w.q_row + T);
+      }
     }
     const int64_t head_off = (int64_t)w.kv_head * p.stride_head_b;
     const int c = lane & 15;  // 16-byte chunk of the 256-byte row
@@ -167,7 +175,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, WAIT_LIMIT));
       if (!ok) break;
       const uint32_t dst0 = s_base + st * TILE_B + half * HALF_B;
-#pragma unroll
+#pragma unroll 8
       for (int i = 0; i < 32; ++i) {
         const int rr = 2 * i + (lane >> 4);  // row within this warp's 64
         const int slot = __shfl_sync(0xffffffffu, i < 16 ? slot_a : slot_b, rr & 31);
@@ -200,60 +208,67 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, KT, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, true);
-      bool ok = tc::mbar_wait(BAR(B_Q), 0, abort_flag, WAIT_LIMIT);
-      tc::fence_after_sync();
-      // Issue S_j = Q K_j^T as soon as K_j has landed and its score buffer is free, and
-      // O += P_j V_j as soon as P_j and V_j are ready (in tile order each), polling both so
-      // neither waits behind the other's inputs.
-      int js = 0, jp = 0;  // next S tile, next PV tile
-      long long t0 = clock64();
-      while (ok && jp < nkt) {
-        bool progressed = false;
-        if (js < nkt && js <= jp + 1) {
-          const int st = js & 1;
-          const uint32_t ph = (js >> 1) & 1;
-          if (tc::mbar_try_wait(BAR(B_KF + st), ph) && tc::mbar_try_wait(BAR(B_SE + st), ph ^ 1)) {
-            tc::fence_proxy_async_smem();
-            tc::fence_after_sync();
-            const uint32_t d = tmem + (uint32_t)st * KT;
+      auto issue_s = [&](int x, int st) {  // S_x = Q_x K_st^T into TMEM columns [128 x, 128 x + 128)
+        const uint32_t d = tmem + (uint32_t)x * 128;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t off = (ks >> 2) * HALF_B + (ks & 3) * 32;
-              const uint64_t a = tc::smem_desc_sw128(sQ + off, 16, 1024);
-              const uint64_t b = tc::smem_desc_sw128(sK + st * TILE_B + off, 16, 1024);
-              tc::mma_bf16_ss(d, a, b, idesc_qk, ks > 0 ? 1u : 0u);
-            }
-            tc::commit(BAR(B_SF + st));
-            tc::commit(BAR(B_KE + st));
-            ++js;
-            progressed = true;
-          }
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * HALF_B + (ks & 3) * 32;
+          const uint64_t a = tc::smem_desc_sw128(sQ + x * TILE_B + off, 16, 1024);
+          const uint64_t b = tc::smem_desc_sw128(sK + st * TILE_B + off, 16, 1024);
+          tc::mma_bf16_ss(d, a, b, idesc_qk, ks > 0 ? 1u : 0u);
         }
-        if (jp < js) {
-          const int st = jp & 1;
-          const uint32_t ph = (jp >> 1) & 1;
-          if (tc::mbar_try_wait(BAR(B_PF), jp & 1) && tc::mbar_try_wait(BAR(B_VF + st), ph)) {
-            tc::fence_proxy_async_smem();
-            tc::fence_after_sync();
+        tc::commit(BAR(B_SF + x));
+      };
+      auto issue_pv = [&](int x, int st, bool first) {  // O_x += P_x V_st, P_x from TMEM
+        const uint32_t a0 = tmem + (uint32_t)x * 128;
+        const uint32_t d = tmem + TMEM_O + (uint32_t)x * 128;
 #pragma unroll
-            for (int kk = 0; kk < KT / 16; ++kk) {
-              const uint64_t a = tc::smem_desc_sw128(sP + (kk >> 2) * HALF_B + (kk & 3) * 32, 16, 1024);
-              const uint64_t b = tc::smem_desc_sw128(sV + st * TILE_B + kk * 2048, HALF_B, 1024);
-              tc::mma_bf16_ss(tmem + TMEM_O, a, b, idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc::commit(BAR(B_OD));
-            tc::commit(BAR(B_VE + st));
-            ++jp;
-            progressed = true;
-          }
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          const uint64_t b = tc::smem_desc_sw128(sV + st * TILE_B + kk * 2048, HALF_B, 1024);
+          tc::mma_bf16_ts(d, a0 + kk * 8, b, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
-        if (progressed) {
-          t0 = clock64();
-        } else if (*abort_flag || clock64() - t0 > WAIT_LIMIT) {
-          ok = false;
-        }
+      };
+      auto wait = [&](uint32_t bar, uint32_t parity) {
+        return tc::mbar_wait(bar, parity, abort_flag, WAIT_LIMIT);
+      };
+      bool ok = wait(BAR(B_Q), 0) && wait(BAR(B_KF), 0);
+      if (ok) {
+        tc::fence_proxy_async_smem();
+        tc::fence_after_sync();
+        issue_s(0, 0);
+        if (two) issue_s(1, 0);
+        tc::commit(BAR(B_KE));
       }
-      if (!ok) {
+      for (int j = 0; j < nkt && ok; ++j) {
+        const int st = j & 1, st1 = (j + 1) & 1;
+        const uint32_t ph = (j >> 1) & 1, ph1 = ((j + 1) >> 1) & 1;
+        const bool more = j + 1 < nkt;
+        ok = wait(BAR(B_PF + 0), j & 1) && wait(BAR(B_VF + st), ph);
+        if (!ok) break;
+        tc::fence_proxy_async_smem();
+        tc::fence_after_sync();
+        issue_pv(0, st, j == 0);
+        if (more) {
+          ok = wait(BAR(B_KF + st1), ph1);
+          if (!ok) break;
+          tc::fence_proxy_async_smem();
+          tc::fence_after_sync();
+          issue_s(0, st1);
+        }
+        if (two) {
+          ok = wait(BAR(B_PF + 1), j & 1);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(1, st, j == 0);
+          if (more) issue_s(1, st1);
+        }
+        tc::commit(BAR(B_VE + st));
+        if (more) tc::commit(BAR(B_KE + st1));
+      }
+      if (ok) {
+        tc::commit(BAR(B_OD + 0));
+        tc::commit(BAR(B_OD + 1));
+      } else {
         *abort_flag = 1;
         record_error(err, PKV_DEVERR_TIMEOUT);
         // every MMA issued so far must be complete before the TMEM is freed
@@ -263,59 +278,48 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------------ softmax (warps 0-7)
+  } else if (warp < 4 || two) {
+    // ------------------------------------------------------------------ softmax (tile A: warps 0-3, B: 4-7)
+    const int x = warp >> 2;  // which Q tile
     const int quarter = warp & 3;
-    const int ch = warp >> 2;                 // key-column half of every tile
-    const int r = quarter * 32 + lane;        // query row == TMEM lane
-    const int t = r / G;
-    const int g = r - t * G;
+    const int r = quarter * 32 + lane;  // row of the tile == TMEM lane
+    const int t = x * T + r / G;        // token of the item
+    const int g = r - (r / G) * G;
     const bool row_valid = t < w.q_rows;
-    const int pos0 = ri.kv_len - ri.q_len + (w.q_row - ri.q_begin);  // position of the tile's first token
+    const int pos0 = ri.kv_len - ri.q_len + (w.q_row - ri.q_begin);  // position of the item's first token
     const int P = pos0 + min(t, w.q_rows - 1);
     const int lo = p.window_left >= 0 ? max(0, P - p.window_left) : 0;
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t col_half = (uint32_t)ch * 64;
+    const uint32_t tS = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)x * 128;
+    const uint32_t tO = tS + TMEM_O;
     const float sc = p.scale_log2;
-    float* xch = reinterpret_cast<float*>(sbase + OFF_XCH);  // [2][2][128] maxima, then [2][128] sums
     float m_used = -INFINITY;
-    float l = 0.f;  // this half's share of the row sum
+    float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
-      const int sb = j & 1;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_SF + sb), (j >> 1) & 1, abort_flag, WAIT_LIMIT));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_SF + x), j & 1, abort_flag, WAIT_LIMIT));
       if (!ok) break;
       tc::fence_after_sync();
-      uint32_t v[64];
-      tc::tmem_ld64(tmem + lane_base + (uint32_t)sb * KT + col_half, v);
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(BAR(B_SE + sb));
-
-      // raw-score maximum over the visible columns of this half (the scale is positive)
-      const int k0 = w.kv_begin + j * KT + ch * 64;
+      const int k0 = w.kv_begin + j * KT;
       const int hi_c = P - k0, lo_c = lo - k0;  // visible columns: lo_c <= c <= hi_c
-      const bool full = __all_sync(0xffffffffu, hi_c >= 63 && lo_c <= 0);
+      const bool full = __all_sync(0xffffffffu, hi_c >= KT - 1 && lo_c <= 0);
+      // pass 1: row maximum of the raw scores (the scale is positive)
       float ma[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
-      } else {
+      for (int h = 0; h < 4; ++h) {
+        uint32_t v[32];
+        tc::tmem_ld32(tS + h * 32, v);
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          if (c > hi_c || c < lo_c) v[c] = __float_as_uint(-INFINITY);
-          ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
+          for (int c = 0; c < 32; ++c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int cc = h * 32 + c;
+            if (cc <= hi_c && cc >= lo_c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
+          }
         }
       }
-      float mx = fmaxf(fmaxf(ma[0], ma[1]), fmaxf(ma[2], ma[3])) * sc;
-      // share the maximum with the partner warp holding the other 64 columns of the same rows
-      xch[(sb * 2 + ch) * 128 + r] = mx;
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(BAR(B_XM + quarter * 2 + sb));
-      ok = __all_sync(0xffffffffu,
-                      tc::mbar_wait(BAR(B_XM + quarter * 2 + sb), (j >> 1) & 1, abort_flag, WAIT_LIMIT));
-      if (!ok) break;
-      mx = fmaxf(mx, xch[(sb * 2 + (ch ^ 1)) * 128 + r]);
+      const float mx = fmaxf(fmaxf(ma[0], ma[1]), fmaxf(ma[2], ma[3])) * sc;
       float corr = 1.f;
       bool rescale = false;
       if (mx > m_used + RESCALE_THRESHOLD) {
@@ -324,79 +328,69 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         l *= corr;
         rescale = true;
       }
+      // O_X is stable here: S_X(j) completing implies PV_X(j-1) completed
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + c4 * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+          tc::tmem_st32(tO + c4 * 32, o);
+        }
+      }
+      // pass 2: P = 2^(s * sc - m) as bf16 pairs, stored over the scores already read
       const float nref = m_used == -INFINITY ? 0.f : -m_used;
       float sa[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(v[2 * c]), sc, nref));
-        const float p1 = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sc, nref));
-        sa[c & 3] += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
+      for (int h = 0; h < 4; ++h) {
+        uint32_t v[32];
+        tc::tmem_ld32(tS + h * 32, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float s0 = __uint_as_float(v[2 * c]), s1 = __uint_as_float(v[2 * c + 1]);
+          if (!full) {
+            const int cc = h * 32 + 2 * c;
+            if (!(cc <= hi_c && cc >= lo_c)) s0 = -INFINITY;
+            if (!(cc + 1 <= hi_c && cc + 1 >= lo_c)) s1 = -INFINITY;
+          }
+          const float p0 = ex2(fmaf(s0, sc, nref));
+          const float p1 = ex2(fmaf(s1, sc, nref));
+          sa[c & 3] += p0 + p1;
+          pk[c] = pack_bf16(p0, p1);
+        }
+        tc::tmem_st16(tS + h * 16, pk);
       }
       l += (sa[0] + sa[1]) + (sa[2] + sa[3]);
-
-      // PV of the previous tile must be complete: O is stable and the P buffer is free
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD), (j - 1) & 1, abort_flag, WAIT_LIMIT));
-        if (!ok) break;
-        tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, rescale)) {
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(BAR(B_PF + x));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD + x), 0, abort_flag, WAIT_LIMIT));
+    if (ok) {
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int head = w.kv_head * G + g;
+      const int64_t row = (int64_t)(w.q_row + t);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D);
 #pragma unroll
-          for (int c4 = 0; c4 < 2; ++c4) {
-            uint32_t o[32];
-            const uint32_t ta = tmem + lane_base + TMEM_O + col_half + c4 * 32;
-            tc::tmem_ld32(ta, o);
+      for (int h = 0; h < 4; ++h) {
+        uint32_t o[32];
+        tc::tmem_ld32(tO + h * 32, o);
+        if (row_valid) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-            tc::tmem_st32(ta, o);
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+            u.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+            u.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+            u.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            dst[h * 4 + q] = u;
           }
         }
       }
-      // this half of the P row -> swizzled K-major bf16 tile
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const uint32_t addr = sP + ch * HALF_B + r * 128 + ((c8 ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(pk[4 * c8]),
-                     "r"(pk[4 * c8 + 1]), "r"(pk[4 * c8 + 2]), "r"(pk[4 * c8 + 3])
-                     : "memory");
-      }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(BAR(B_PF));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD), (nkt - 1) & 1, abort_flag, WAIT_LIMIT));
-    if (ok) {
-      // full row sum from the two halves
-      float* xl = xch + 2 * 2 * 128;
-      xl[ch * 128 + r] = l;
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(BAR(B_XL + quarter));
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_XL + quarter), 0, abort_flag, WAIT_LIMIT));
-    }
-    if (ok) {
-      const float lt = l + xch[2 * 2 * 128 + (ch ^ 1) * 128 + r];
-      tc::fence_after_sync();
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const int head = w.kv_head * G + g;
-      const int64_t row = (int64_t)(w.q_row + t);
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D +
-                                            ch * 64);
-      uint32_t o[64];
-      tc::tmem_ld64(tmem + lane_base + TMEM_O + col_half, o);
-      if (row_valid) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint4 u;
-          u.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          u.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          u.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          u.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-          dst[q] = u;
-        }
-        if (ch == 0 && p.lse) p.lse[row * p.num_qo_heads + head] = (m_used + __log2f(lt)) * 0.69314718055994531f;
-      }
+      if (row_valid && p.lse) p.lse[row * p.num_qo_heads + head] = (m_used + __log2f(l)) * 0.69314718055994531f;
     } else {
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
