@@ -11,13 +11,13 @@
 // GB300 design.  One CTA = two 128-row query tiles (A and B: consecutive tokens of one request, rows
 // = (token, head) pairs of one KV head's query-head group) sharing every K/V tile, so each gathered
 // K/V byte feeds twice the tensor-core work of a single tile:
-//  * warps 9-12 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps 9-10) and V
-//    (warps 11-12) tiles of 128 keys gathered row by row through the page table with 16-byte
+//  * warps 8-11 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps 8-9) and V
+//    (warps 10-11) tiles of 128 keys gathered row by row through the page table with 16-byte
 //    cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the tensor core
 //    reads; two stages; each producer thread waits for its own copies, fences them into the async
 //    proxy and arrives on the stage's mbarrier.  (TMA tile::gather4 moves 512 bytes per instruction
 //    and measured slower here for token-granular pools.)
-//  * warp 8 (MMA): one thread issues tcgen05.mma (kind::f16, M=128, N=128, K=16, bf16 in, fp32
+//  * warp 12 (MMA): one thread issues tcgen05.mma (kind::f16, M=128, N=128, K=16, bf16 in, fp32
 //    accumulate in TMEM) in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ..., so the
 //    tensor core works on one tile while the other tile's softmax runs.  P lives in TMEM on top of
 //    its own scores and is the A operand of the PV MMA (V is an MN-major shared-memory operand, no
@@ -29,7 +29,8 @@
 //    scores already consumed.  Causal / window masking only on tiles that need it.  The row maximum
 //    moves lazily (only when it grows by more than 2^8; exact because numerator and denominator
 //    share it), and O is rescaled in TMEM only then.  Epilogue: O / l to bf16 rows and the LSE.
-// Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its own
+// Registers are rebalanced with setmaxnreg: the two softmax warpgroups take 176 per thread, the
+// producer and MMA warpgroups keep 80.  Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its own
 // copies and MMAs, frees its TMEM and exits.
 
 #include <cuda.h>
@@ -70,15 +71,19 @@ enum {
 };
 constexpr uint32_t TMEM_COLS = 512;  // S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384), O_B [384,512)
 constexpr uint32_t TMEM_O = 256;
-constexpr int THREADS = 416;          // 8 softmax warps, 1 MMA warp, 4 producer warps
-constexpr int MMA_WARP = 8;
-constexpr int PRODUCER_WARP0 = 9;
+constexpr int THREADS = 512;          // 4 warpgroups: softmax A, softmax B, producers, MMA (+3 idle warps)
+constexpr int PRODUCER_WARP0 = 8;     // warps 8-9 gather K, 10-11 gather V
+constexpr int MMA_WARP = 12;
+// launched at 65536 / 512 = 128 registers per thread, then rebalanced per warpgroup:
+// 2 x 128 x SOFTMAX_REGS + 2 x 128 x OTHER_REGS = 45056 + 20480 = 65536 <= 65536
+constexpr uint32_t SOFTMAX_REGS = 176;
+constexpr uint32_t OTHER_REGS = 80;
 constexpr int PRODUCER_THREADS = 64;  // per operand (K or V)
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 }  // namespace pf
 
-__global__ void __maxnreg__(152)
+__global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, int32_t* err) {
   using namespace pf;
@@ -127,8 +132,12 @@ __global__ void __maxnreg__(152)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if (warp < 8)
+    tc::reg_alloc<SOFTMAX_REGS>();
+  else
+    tc::reg_dealloc<OTHER_REGS>();
 
-  if (warp >= PRODUCER_WARP0) {
+  if (warp >= PRODUCER_WARP0 && warp < PRODUCER_WARP0 + 4) {
     // ------------------------------------------------------------------ producers (cp.async)
     const bool is_k = warp < PRODUCER_WARP0 + 2;
     const int pw = (warp - PRODUCER_WARP0) & 1;  // which 64-row half of the K/V tile this warp fills
@@ -278,7 +287,7 @@ __global__ void __maxnreg__(152)
       }
     }
     __syncwarp();
-  } else if (warp < 4 || two) {
+  } else if (warp < 4 || (warp < 8 && two)) {
     // ------------------------------------------------------------------ softmax (tile A: warps 0-3, B: 4-7)
     const int x = warp >> 2;  // which Q tile
     const int quarter = warp & 3;
