@@ -23,10 +23,10 @@
 //    its own scores and is the A operand of the PV MMA (V is an MN-major shared-memory operand, no
 //    transpose).  MMAs of one thread execute in issue order, so S_X(j+1) overwriting P_X(j) is safe
 //    once PV_X(j) was issued, and "S_X(j) complete" implies "PV_X(j-1) complete".
-//  * warps 0-3 / 4-7 (softmax of tile A / B): thread r owns row r (TMEM lane r).  Pass 1 reads the
-//    128 scores in 32-column loads for the row maximum; pass 2 re-reads them, computes
-//    p = 2^(s * scale * log2 e - m) with one FFMA + ex2, packs bf16 pairs and stores them over the
-//    scores already consumed.  Causal / window masking only on tiles that need it.  The row maximum
+//  * warps 0-3 / 4-7 (softmax of tile A / B): thread r owns row r (TMEM lane r).  All 128 scores of
+//    the row come into registers with four TMEM loads and one wait; then the row maximum,
+//    p = 2^(s * scale * log2 e - m) with one FFMA + ex2, bf16 pairs packed in place and stored over
+//    the scores with one 64-column TMEM store.  Causal / window masking only on tiles that need it.  The row maximum
 //    moves lazily (only when it grows by more than 2^8; exact because numerator and denominator
 //    share it), and O is rescaled in TMEM only then.  Epilogue: O / l to bf16 rows and the LSE.
 // Registers are rebalanced with setmaxnreg: the two softmax warpgroups take 176 per thread, the
@@ -132,13 +132,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 8)
-    tc::reg_alloc<SOFTMAX_REGS>();
-  else
-    tc::reg_dealloc<OTHER_REGS>();
 
   if (warp >= PRODUCER_WARP0 && warp < PRODUCER_WARP0 + 4) {
     // ------------------------------------------------------------------ producers (cp.async)
+    tc::reg_dealloc<OTHER_REGS>();
     const bool is_k = warp < PRODUCER_WARP0 + 2;
     const int pw = (warp - PRODUCER_WARP0) & 1;  // which 64-row half of the K/V tile this warp fills
     const char* pool = is_k ? p.k_pool : p.v_pool;
@@ -212,9 +209,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp >= MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer (warps 13-15 idle)
+    tc::reg_dealloc<OTHER_REGS>();
+    if (warp == MMA_WARP && lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, KT, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, true);
       auto issue_s = [&](int x, int st) {  // S_x = Q_x K_st^T into TMEM columns [128 x, 128 x + 128)
@@ -287,8 +285,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 4 || (warp < 8 && two)) {
+  } else {
     // ------------------------------------------------------------------ softmax (tile A: warps 0-3, B: 4-7)
+    tc::reg_alloc<SOFTMAX_REGS>();
+    if (warp < 4 || two) {
     const int x = warp >> 2;  // which Q tile
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row of the tile == TMEM lane
@@ -311,23 +311,18 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       const int k0 = w.kv_begin + j * KT;
       const int hi_c = P - k0, lo_c = lo - k0;  // visible columns: lo_c <= c <= hi_c
       const bool full = __all_sync(0xffffffffu, hi_c >= KT - 1 && lo_c <= 0);
-      // pass 1: row maximum of the raw scores (the scale is positive)
+      // all 128 scores of the row in registers: four TMEM loads in flight, one wait
+      uint32_t v[KT];
+      tc::tmem_ld128(tS, v);
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < KT; ++c)
+          if (!(c <= hi_c && c >= lo_c)) v[c] = __float_as_uint(-INFINITY);
+      }
+      // row maximum of the raw scores (the scale is positive)
       float ma[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t v[32];
-        tc::tmem_ld32(tS + h * 32, v);
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int cc = h * 32 + c;
-            if (cc <= hi_c && cc >= lo_c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
-          }
-        }
-      }
+      for (int c = 0; c < KT; ++c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
       const float mx = fmaxf(fmaxf(ma[0], ma[1]), fmaxf(ma[2], ma[3])) * sc;
       float corr = 1.f;
       bool rescale = false;
@@ -337,7 +332,19 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         l *= corr;
         rescale = true;
       }
-      // O_X is stable here: S_X(j) completing implies PV_X(j-1) completed
+      // P = 2^(s * sc - m) as bf16 pairs, packed in place and stored over the scores
+      const float nref = m_used == -INFINITY ? 0.f : -m_used;
+      float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < KT / 2; ++c) {
+        const float p0 = ex2(fmaf(__uint_as_float(v[2 * c]), sc, nref));
+        const float p1 = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sc, nref));
+        sa[c & 3] += p0 + p1;
+        v[c] = pack_bf16(p0, p1);
+      }
+      tc::tmem_st64(tS, *reinterpret_cast<const uint32_t(*)[64]>(v));
+      // O_X is stable here (S_X(j) completing implies PV_X(j-1) completed), and PV_X(j) cannot start
+      // before this warp signals P_X(j) below: rescale O_X now if the reference maximum moved
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
         for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -347,29 +354,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
           tc::tmem_st32(tO + c4 * 32, o);
         }
-      }
-      // pass 2: P = 2^(s * sc - m) as bf16 pairs, stored over the scores already read
-      const float nref = m_used == -INFINITY ? 0.f : -m_used;
-      float sa[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t v[32];
-        tc::tmem_ld32(tS + h * 32, v);
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float s0 = __uint_as_float(v[2 * c]), s1 = __uint_as_float(v[2 * c + 1]);
-          if (!full) {
-            const int cc = h * 32 + 2 * c;
-            if (!(cc <= hi_c && cc >= lo_c)) s0 = -INFINITY;
-            if (!(cc + 1 <= hi_c && cc + 1 >= lo_c)) s1 = -INFINITY;
-          }
-          const float p0 = ex2(fmaf(s0, sc, nref));
-          const float p1 = ex2(fmaf(s1, sc, nref));
-          sa[c & 3] += p0 + p1;
-          pk[c] = pack_bf16(p0, p1);
-        }
-        tc::tmem_st16(tS + h * 16, pk);
       }
       l += (sa[0] + sa[1]) + (sa[2] + sa[3]);
       tc::fence_before_sync();
@@ -403,6 +387,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     } else {
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
+    }
     }
   }
 
