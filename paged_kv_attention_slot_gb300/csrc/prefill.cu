@@ -14,8 +14,9 @@
 //  * warps 8-11 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps 8-9) and V
 //    (warps 10-11) tiles of 128 keys gathered row by row through the page table with 16-byte
 //    cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the tensor core
-//    reads; two stages; each producer thread waits for its own copies, fences them into the async
-//    proxy and arrives on the stage's mbarrier.  (TMA tile::gather4 moves 512 bytes per instruction
+//    reads; two stages; each producer thread's arrival on the stage's mbarrier is posted by the
+//    hardware when its copies land (cp.async.mbarrier.arrive.noinc), so a tile is announced as
+//    soon as it is in shared memory; the MMA thread fences it into the async proxy after its wait.  (TMA tile::gather4 moves 512 bytes per instruction
 //    and measured slower here for token-granular pools.)
 //  * warp 12 (MMA): one thread issues tcgen05.mma (kind::f16, M=128, N=128, K=16, bf16 in, fp32
 //    accumulate in TMEM) in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ..., so the
@@ -166,7 +167,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       return page * p.page_size + (key - lp * p.page_size);
     };
     bool ok = true;
-    int pending = 0;  // tiles issued whose arrival is still owed
     // slot rows of the next tile are loaded one iteration ahead so their latency overlaps the copies
     int next_a = slot_of(w.kv_begin + pw * 64 + lane);
     int next_b = slot_of(w.kv_begin + pw * 64 + 32 + lane);
@@ -190,21 +190,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         const char* src = pool + (slot >= 0 ? (int64_t)slot * p.stride_token_b + head_off + c * 16 : 0);
         cp_async16(dst, src, slot >= 0 ? 16u : 0u);
       }
-      cp_async_commit();
-      ++pending;
-      if (j > 0) {
-        // this thread's copies of tile j-1 have landed: publish them to the tensor core
-        cp_async_wait<1>();
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(full0 + 8 * ((j - 1) & 1));
-        --pending;
-      }
+      // the stage's barrier receives this thread's arrival when its copies have landed; the MMA
+      // thread fences them into the async proxy after its wait
+      cp_async_arrive_noinc(full0 + 8 * st);
     }
-    cp_async_wait<0>();
-    if (pending > 0 && ok) {
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(full0 + 8 * ((nkt - 1) & 1));
-    }
+    cp_async_wait_all();
     if (!ok) {
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
