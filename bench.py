@@ -388,7 +388,7 @@ def prefill_measure(device, steps, warmup, peak_tflops):
         "flops_per_step": flops,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tflops, 4),
-                     "traffic": _traffic("prefill", ["prefill.cu", "ptx.cuh"])},
+                     "traffic": _traffic("prefill", ["prefill.cu", "ptx.cuh", "tc.cuh"])},
         "run_ms_mean": round(run_avg, 4),
         "gpu_launches_per_step": 2,
     }
