@@ -46,8 +46,6 @@ int fail(int code, const std::string& msg) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Decode kernel occupancy assumed by the split policy (it is launched with 2 CTAs per SM).
-constexpr int kDecodeCtasPerSm = 2;
 constexpr int kDecodeWaves = 1;          // chunk = total work / (SMs * CTAs/SM * waves)
 constexpr int kDecodeMinChunk = 256;     // never split below this many keys
 constexpr int kDecodeChunkAlign = 64;    // 4 warps x 16 keys
@@ -215,7 +213,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     if (a->max_splits == 1) {
       chunk = INT32_MAX;
     } else {
-      const int64_t target = (int64_t)sms * kDecodeCtasPerSm * kDecodeWaves;
+      const int64_t target = (int64_t)sms * pkv::decode_ctas_per_sm(a->kv_dtype, a->head_dim, G) * kDecodeWaves;
       chunk = (work_total + target - 1) / std::max<int64_t>(1, target);
       chunk = std::max<int64_t>(chunk, kDecodeMinChunk);
       chunk = align_up(chunk, kDecodeChunkAlign);

@@ -8,20 +8,23 @@
 // small matrix products and tensor cores pay).
 //
 // GB300 design.  Decode is HBM-bound (about G flops per byte of KV), so the kernel is built around
-// streaming the pages at full bandwidth:
-//  * one CTA = 4 warps = one work item (request, KV head, head group of <= 16 query heads, KV chunk);
-//    the planner cuts long sequences into equal chunks and launches CTAs longest first;
+// streaming the pages at full bandwidth while keeping the per-key work short:
+//  * one CTA = 4 warps = one work item (request, KV head, group of <= 16 query heads, KV chunk); the
+//    planner cuts long sequences into equal chunks and launches CTAs longest first;
 //  * every warp runs its own cp.async ring (16 keys per stage, K and V rows gathered page by page
 //    through kv_indices, 16-byte vectors, XOR-swizzled so ldmatrix reads are conflict-free) and takes
 //    every 4th 16-key tile of the chunk, so no CTA-wide barrier sits in the main loop;
-//  * the query heads of one KV head are packed into the M dimension of an m16n8k16 tensor-core MMA,
-//    so each K/V row is read from HBM exactly once per KV head; S = Q K^T and O += P V both run on
-//    the tensor cores with fp32 accumulation, and the online softmax lives in the MMA fragments
-//    (warp shuffles across the 4 lanes of a row);
-//  * FP8 (E4M3) pages are widened to f16 in registers (exact), the K scale is folded into the score
-//    scale and the V scale into the output; for FP8 the head-dim order inside each 16-element block
-//    is permuted identically for Q and K (a sum does not depend on order) so that one ldmatrix feeds
-//    two code bytes per register half directly;
+//  * the products run on m16n8k16 tensor-core MMAs with the KEYS in M and the (<= 8 per n-block)
+//    query heads of one KV head in N: S^T = K Q^T, then O^T += V^T P^T.  Each K/V row is read once
+//    per KV head, a 16-key tile costs 8 MMAs per product (not 16 with heads in M), and the output
+//    accumulator is 32 registers per 8 heads.  P^T goes from the accumulator layout of the first MMA
+//    to the operand layout of the second with one movmatrix.trans per 8x8 block;
+//  * the online softmax runs per head column: a max over the 16 keys of the tile (3 shuffles), base-2
+//    exponentials with the scale folded in, running sums kept per lane and reduced at the end;
+//  * FP8 (E4M3) pages are widened to f16 in registers (exact); the K scale is folded into the score
+//    scale and the V scale into the output; the head-dim order inside each 16-element block is
+//    permuted identically for Q and K (a dot product does not depend on order) so one ldmatrix feeds
+//    two code bytes per register half, and V's byte pairs are split into even/odd head-dim rows;
 //  * the 4 warps merge their softmax states through shared memory at the end; a CTA either writes
 //    the final bf16 output (no split) or a normalised fp32 partial plus its log2-sum-exp; the last
 //    CTA of a split unit to finish (an atomic count per unit, reset after use, no waiting) merges
@@ -37,37 +40,42 @@ namespace pkv {
 
 int32_t* device_error_ptr();
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NB>
 struct DecodeCfg {
   static constexpr int ROWB = FP8 ? D : 2 * D;  // bytes per key row of one head
   static constexpr int CH = ROWB / 16;          // 16-byte chunks per row
   static constexpr int KEYS = 16;               // keys per warp tile
   static constexpr int TILE_B = KEYS * ROWB;    // bytes of one K (or V) tile
-  static constexpr int STAGES = (2 * TILE_B <= 4096) ? 6 : 3;
+  static constexpr int HEADS = 8 * NB;          // query heads per CTA (n dimension)
+  static constexpr int STAGES = 3;
   static constexpr int WARPS = 4;
+  // resident CTAs per SM: the 8-KB-per-stage bf16/D128 variant fits 2 (shared memory), the 4-KB
+  // variants fit 4 when the accumulators are for 8 heads (registers)
+  static constexpr int CTAS = (2 * TILE_B > 4096 || NB > 1) ? 2 : 4;
   static constexpr int WARP_SMEM = STAGES * 2 * TILE_B;
   static constexpr int PIPE_SMEM = WARPS * WARP_SMEM;
-  static constexpr int MERGE_SMEM = (WARPS * kDecodeRows * D + 2 * WARPS * kDecodeRows + WARPS * kDecodeRows) * 4;
+  static constexpr int MERGE_SMEM = (WARPS * HEADS * D + 3 * WARPS * HEADS) * 4;
   static constexpr int SMEM = PIPE_SMEM > MERGE_SMEM ? PIPE_SMEM : MERGE_SMEM;
-  static constexpr int NB = D / 8;   // 8-column n-blocks of O
-  static constexpr int KS = D / 16;  // k-steps of Q K^T
+  static constexpr int MB = D / 16;  // 16-row m-blocks of O^T
+  static constexpr int KS = D / 16;  // k-steps of S^T
   static_assert(CH >= 8, "rows must span at least 8 chunks for the XOR swizzle");
+  static_assert(SMEM * CTAS <= 232448, "shared memory per SM");
 };
 
-// Column (head-dim index) of accumulator element j (0..3) of O n-block nb for lane quad t.
+// Head-dim index of accumulator element j (0..3) of O^T m-block mb, lane row g.
 template <bool FP8>
-__device__ __forceinline__ int o_col(int nb, int j, int t) {
+__device__ __forceinline__ int o_dim(int mb, int j, int g) {
   if constexpr (!FP8) {
-    return nb * 8 + 2 * t + (j & 1);
+    return mb * 16 + g + 8 * (j >> 1);
   } else {
-    // n-block nb = 2 * chunk + parity covers head dims 16 * chunk + 2 n + parity
-    return (nb >> 1) * 16 + 4 * t + 2 * (j & 1) + (nb & 1);
+    // m-block mb = 2 q + parity: rows g -> dims 32 q + 2 g + parity, rows g + 8 -> 32 q + 16 + 2 g + parity
+    return (mb >> 1) * 32 + 16 * (j >> 1) + 2 * g + (mb & 1);
   }
 }
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32_t* err) {
-  using C = DecodeCfg<D, FP8>;
+template <int D, bool FP8, int NB>
+__global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kernel(const RunParams p, int32_t* err) {
+  using C = DecodeCfg<D, FP8, NB>;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const WorkItem w = p.work[blockIdx.x];
@@ -77,35 +85,25 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
   const int g = lane >> 2;
   const int t = lane & 3;
   const int qh0 = w.kv_head * p.group + w.head_group * kDecodeRows;
-  const int rows = min(kDecodeRows, p.group - w.head_group * kDecodeRows);
+  const int rows = min(C::HEADS, p.group - w.head_group * kDecodeRows);
 
-  // ---- Q fragments (A operand, rows = query heads of this group, zero beyond `rows`) ----
-  uint32_t qa[C::KS][4];
-  {
-    const uint16_t* qb = static_cast<const uint16_t*>(p.q) + ((int64_t)w.q_row * p.num_qo_heads + qh0) * D;
-    const uint16_t* r0 = qb + (int64_t)g * D;
-    const uint16_t* r1 = qb + (int64_t)(g + 8) * D;
-    const bool v0 = g < rows, v1 = g + 8 < rows;
+  // ---- Q^T fragments (B operand: k = head dim, n = query head g of each n-block) ----
+  uint32_t qb[C::KS][NB][2];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    const int head = nb * 8 + g;
+    const bool valid = head < rows;
+    const uint16_t* qr = static_cast<const uint16_t*>(p.q) + ((int64_t)w.q_row * p.num_qo_heads + qh0 + head) * D;
 #pragma unroll
     for (int ks = 0; ks < C::KS; ++ks) {
       if constexpr (!FP8) {
-        const int c0 = ks * 16 + 2 * t;
-        qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + c0) : 0u;
-        qa[ks][1] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + c0) : 0u;
-        qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t*>(r0 + c0 + 8) : 0u;
-        qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t*>(r1 + c0 + 8) : 0u;
+        qb[ks][nb][0] = valid ? *reinterpret_cast<const uint32_t*>(qr + ks * 16 + 2 * t) : 0u;
+        qb[ks][nb][1] = valid ? *reinterpret_cast<const uint32_t*>(qr + ks * 16 + 8 + 2 * t) : 0u;
       } else {
         // permuted order: logical k {2t, 2t+1} <- dims 16ks+4t+{0,1}; {2t+8, 2t+9} <- 16ks+4t+{2,3}
-        const int c0 = ks * 16 + 4 * t;
-        uint2 x0 = v0 ? *reinterpret_cast<const uint2*>(r0 + c0) : make_uint2(0, 0);
-        uint2 x1 = v1 ? *reinterpret_cast<const uint2*>(r1 + c0) : make_uint2(0, 0);
-        auto cv = [](uint32_t two_bf16) {
-          return pack_f16(__uint_as_float(two_bf16 << 16), __uint_as_float(two_bf16 & 0xffff0000u));
-        };
-        qa[ks][0] = cv(x0.x);
-        qa[ks][1] = cv(x1.x);
-        qa[ks][2] = cv(x0.y);
-        qa[ks][3] = cv(x1.y);
+        const uint2 x = valid ? *reinterpret_cast<const uint2*>(qr + ks * 16 + 4 * t) : make_uint2(0, 0);
+        qb[ks][nb][0] = pack_f16(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
+        qb[ks][nb][1] = pack_f16(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
       }
     }
   }
@@ -156,11 +154,15 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
     }
   };
 
-  float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 units) of rows g and g + 8
-  float l0 = 0.f, l1 = 0.f;              // running sums (this lane's columns only)
-  float o[C::NB][4];
+  float m[NB][2], l[NB][2];  // per head column 2t, 2t+1: running max (log2 units) and this lane's sum
+  float o[C::MB][NB][4];     // O^T: rows = head dims, columns = heads
 #pragma unroll
-  for (int nb = 0; nb < C::NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+  for (int nb = 0; nb < NB; ++nb) {
+    m[nb][0] = m[nb][1] = -INFINITY;
+    l[nb][0] = l[nb][1] = 0.f;
+#pragma unroll
+    for (int mb = 0; mb < C::MB; ++mb) o[mb][nb][0] = o[mb][nb][1] = o[mb][nb][2] = o[mb][nb][3] = 0.f;
+  }
 
 #pragma unroll
   for (int s = 0; s < C::STAGES - 1; ++s) {
@@ -168,10 +170,10 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
     cp_async_commit();
   }
 
-  // ldmatrix lane roles
+  // ldmatrix lane roles: K as the A operand (rows = keys), V^T as the A operand (.trans, rows = dims)
   const int mi = lane >> 3, rr = lane & 7;
-  const int k_key = FP8 ? (((mi & 1) << 3) + rr) : (((mi >> 1) << 3) + rr);
-  const int v_key = ((mi & 1) << 3) + rr;
+  const int k_key = ((mi & 1) << 3) + rr;  // matrices: (keys 0-7, c), (keys 8-15, c), (keys 0-7, c+1), (8-15, c+1)
+  const int v_key = ((mi >> 1) << 3) + rr; // matrices: (keys 0-7, c), (keys 0-7, c+1), (keys 8-15, c), (8-15, c+1)
 
   for (int i = 0; i < my_tiles; ++i) {
     cp_async_wait<C::STAGES - 2>();
@@ -181,107 +183,106 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
     const uint32_t vb = kb + C::TILE_B;
     const int key0 = w.kv_begin + (warp + i * C::WARPS) * C::KEYS;
 
-    // ---- S = Q K^T for 16 keys (two n-blocks of 8) ----
-    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // ---- S^T = K Q^T for 16 keys ----
+    float s[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
     if constexpr (!FP8) {
 #pragma unroll
       for (int ks = 0; ks < C::KS; ++ks) {
-        uint32_t b[4];
-        const int chunk = 2 * ks + (mi & 1);
-        ldsm_x4(b, kb + k_key * C::ROWB + ((chunk ^ (k_key & 7)) << 4));
-        mma_bf16(s[0], qa[ks], b[0], b[1]);
-        mma_bf16(s[1], qa[ks], b[2], b[3]);
+        uint32_t a[4];
+        const int chunk = 2 * ks + (mi >> 1);
+        ldsm_x4(a, kb + k_key * C::ROWB + ((chunk ^ (k_key & 7)) << 4));
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_bf16(s[nb], a, qb[ks][nb][0], qb[ks][nb][1]);
       }
     } else {
 #pragma unroll
       for (int c = 0; c < C::KS; c += 2) {
-        uint32_t b[4];
+        uint32_t r[4];
         const int chunk = c + (mi >> 1);
-        ldsm_x4(b, kb + k_key * C::ROWB + ((chunk ^ (k_key & 7)) << 4));
-        // b[0]: keys 0-7 / chunk c, b[1]: keys 8-15 / chunk c, b[2], b[3]: chunk c + 1
-        mma_f16(s[0], qa[c], e4m3x2_to_f16x2(b[0] & 0xffffu), e4m3x2_to_f16x2(b[0] >> 16));
-        mma_f16(s[1], qa[c], e4m3x2_to_f16x2(b[1] & 0xffffu), e4m3x2_to_f16x2(b[1] >> 16));
-        mma_f16(s[0], qa[c + 1], e4m3x2_to_f16x2(b[2] & 0xffffu), e4m3x2_to_f16x2(b[2] >> 16));
-        mma_f16(s[1], qa[c + 1], e4m3x2_to_f16x2(b[3] & 0xffffu), e4m3x2_to_f16x2(b[3] >> 16));
+        ldsm_x4(r, kb + k_key * C::ROWB + ((chunk ^ (k_key & 7)) << 4));
+        // r[0]: keys 0-7 / chunk c, r[1]: keys 8-15 / chunk c, r[2], r[3]: chunk c + 1
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t a[4] = {e4m3x2_to_f16x2(r[2 * h] & 0xffffu), e4m3x2_to_f16x2(r[2 * h + 1] & 0xffffu),
+                                 e4m3x2_to_f16x2(r[2 * h] >> 16), e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(s[nb], a, qb[c + h][nb][0], qb[c + h][nb][1]);
+        }
       }
     }
 
-    // ---- online softmax (log2 domain) ----
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    // ---- online softmax per head column (log2 domain) ----
+    const bool lo_ok = key0 + g < w.kv_end, hi_ok = key0 + g + 8 < w.kv_end;
+    uint32_t pb[NB][2];
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+    for (int nb = 0; nb < NB; ++nb) {
+      float x0 = lo_ok ? s[nb][0] * p.scale_log2 : -INFINITY;  // key g,     head 2t
+      float x1 = lo_ok ? s[nb][1] * p.scale_log2 : -INFINITY;  // key g,     head 2t+1
+      float x2 = hi_ok ? s[nb][2] * p.scale_log2 : -INFINITY;  // key g + 8, head 2t
+      float x3 = hi_ok ? s[nb][3] * p.scale_log2 : -INFINITY;  // key g + 8, head 2t+1
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int key = key0 + nb * 8 + 2 * t + (j & 1);
-        s[nb][j] = key < w.kv_end ? s[nb][j] * p.scale_log2 : -INFINITY;
+      for (int sh = 4; sh < 32; sh <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
       }
-      mx0 = fmaxf(mx0, fmaxf(s[nb][0], s[nb][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nb][2], s[nb][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float c0 = ex2(m0 - mn0), c1 = ex2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
+      // every tile holds at least one visible key, so the new maxima are finite
+      const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
+      const float c0 = ex2(m[nb][0] - mn0), c1 = ex2(m[nb][1] - mn1);
+      m[nb][0] = mn0;
+      m[nb][1] = mn1;
+      x0 = ex2(x0 - mn0);
+      x1 = ex2(x1 - mn1);
+      x2 = ex2(x2 - mn0);
+      x3 = ex2(x3 - mn1);
+      l[nb][0] = l[nb][0] * c0 + (x0 + x2);
+      l[nb][1] = l[nb][1] * c1 + (x1 + x3);
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      s[nb][0] = ex2(s[nb][0] - mn0);
-      s[nb][1] = ex2(s[nb][1] - mn0);
-      s[nb][2] = ex2(s[nb][2] - mn1);
-      s[nb][3] = ex2(s[nb][3] - mn1);
-      ps0 += s[nb][0] + s[nb][1];
-      ps1 += s[nb][2] + s[nb][3];
-    }
-    l0 = l0 * c0 + ps0;
-    l1 = l1 * c1 + ps1;
-#pragma unroll
-    for (int nb = 0; nb < C::NB; ++nb) {
-      o[nb][0] *= c0;
-      o[nb][1] *= c0;
-      o[nb][2] *= c1;
-      o[nb][3] *= c1;
+      for (int mb = 0; mb < C::MB; ++mb) {
+        o[mb][nb][0] *= c0;
+        o[mb][nb][1] *= c1;
+        o[mb][nb][2] *= c0;
+        o[mb][nb][3] *= c1;
+      }
+      // P^T in accumulator layout (row = key, column pair = heads) -> B operand (k = keys, n = head)
+      if constexpr (!FP8) {
+        pb[nb][0] = movmatrix_trans(pack_bf16(x0, x1));
+        pb[nb][1] = movmatrix_trans(pack_bf16(x2, x3));
+      } else {
+        pb[nb][0] = movmatrix_trans(pack_f16(x0, x1));
+        pb[nb][1] = movmatrix_trans(pack_f16(x2, x3));
+      }
     }
 
-    // ---- O += P V ----
-    uint32_t pa[4];
+    // ---- O^T += V^T P^T ----
     if constexpr (!FP8) {
-      pa[0] = pack_bf16(s[0][0], s[0][1]);
-      pa[1] = pack_bf16(s[0][2], s[0][3]);
-      pa[2] = pack_bf16(s[1][0], s[1][1]);
-      pa[3] = pack_bf16(s[1][2], s[1][3]);
 #pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        uint32_t b[4];
-        const int chunk = 2 * dn + (mi >> 1);
-        ldsm_x4_t(b, vb + v_key * C::ROWB + ((chunk ^ (v_key & 7)) << 4));
-        mma_bf16(o[2 * dn], pa, b[0], b[1]);
-        mma_bf16(o[2 * dn + 1], pa, b[2], b[3]);
+      for (int mb = 0; mb < C::MB; ++mb) {
+        uint32_t a[4];
+        const int chunk = 2 * mb + (mi & 1);
+        ldsm_x4_t(a, vb + v_key * C::ROWB + ((chunk ^ (v_key & 7)) << 4));
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) mma_bf16(o[mb][nb], a, pb[nb][0], pb[nb][1]);
       }
     } else {
-      pa[0] = pack_f16(s[0][0], s[0][1]);
-      pa[1] = pack_f16(s[0][2], s[0][3]);
-      pa[2] = pack_f16(s[1][0], s[1][1]);
-      pa[3] = pack_f16(s[1][2], s[1][3]);
 #pragma unroll
       for (int c = 0; c < D / 16; c += 2) {
-        uint32_t b[4];
-        const int chunk = c + (mi >> 1);
-        ldsm_x4_t(b, vb + v_key * C::ROWB + ((chunk ^ (v_key & 7)) << 4));
-        // b[0]: keys 0-7 x chunk c, b[1]: keys 8-15 x chunk c, b[2]/b[3]: chunk c + 1.  Each register
-        // holds, for byte pair column g: (key 2t: d, d+1), (key 2t+1: d, d+1) with d = 16 chunk + 2g.
+        uint32_t r[4];
+        const int chunk = c + (mi & 1);
+        ldsm_x4_t(r, vb + v_key * C::ROWB + ((chunk ^ (v_key & 7)) << 4));
+        // r[0]: keys 0-7 x chunk c, r[1]: keys 0-7 x chunk c+1, r[2]: keys 8-15 x chunk c,
+        // r[3]: keys 8-15 x chunk c+1.  Each register holds, for byte-pair column g:
+        // (key 2t: d, d+1), (key 2t+1: d, d+1) with d = 16 chunk + 2g; bytes 0/2 are the even dim,
+        // bytes 1/3 the odd one.
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t lo = b[2 * q], hi = b[2 * q + 1];
-          const uint32_t e0 = e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0020));
-          const uint32_t e1 = e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0020));
-          const uint32_t d0 = e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0031));
-          const uint32_t d1 = e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0031));
-          mma_f16(o[2 * (c + q)], pa, e0, e1);
-          mma_f16(o[2 * (c + q) + 1], pa, d0, d1);
+        for (int par = 0; par < 2; ++par) {
+          const uint32_t sel = par ? 0x0031u : 0x0020u;
+          const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, sel)), e4m3x2_to_f16x2(__byte_perm(r[1], 0, sel)),
+                                 e4m3x2_to_f16x2(__byte_perm(r[2], 0, sel)), e4m3x2_to_f16x2(__byte_perm(r[3], 0, sel))};
+#pragma unroll
+          for (int nb = 0; nb < NB; ++nb) mma_f16(o[c + par][nb], a, pb[nb][0], pb[nb][1]);
         }
       }
     }
@@ -292,49 +293,59 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
   }
   cp_async_wait<0>();
 
-  // full row sums across the 4 lanes of each row
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  // full per-head sums across the 8 key rows g of the warp
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      l[nb][0] += __shfl_xor_sync(0xffffffffu, l[nb][0], sh);
+      l[nb][1] += __shfl_xor_sync(0xffffffffu, l[nb][1], sh);
+    }
+  }
 
   // ---- merge the 4 warps' states through shared memory ----
   __syncthreads();
-  float* so = reinterpret_cast<float*>(smem);                 // [4][16][D]
-  float* sm = so + C::WARPS * kDecodeRows * D;                // [4][16]
-  float* sl = sm + C::WARPS * kDecodeRows;                    // [4][16]
-  float* sf = sl + C::WARPS * kDecodeRows;                    // [4][16] weights
-  if (t == 0) {
-    sm[warp * kDecodeRows + g] = m0;
-    sm[warp * kDecodeRows + g + 8] = m1;
-    sl[warp * kDecodeRows + g] = l0;
-    sl[warp * kDecodeRows + g + 8] = l1;
+  float* so = reinterpret_cast<float*>(smem);   // [4][HEADS][D]
+  float* sm = so + C::WARPS * C::HEADS * D;     // [4][HEADS]
+  float* sl = sm + C::WARPS * C::HEADS;         // [4][HEADS]
+  float* sf = sl + C::WARPS * C::HEADS;         // [4][HEADS] weights
+  if (g == 0) {
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      sm[warp * C::HEADS + nb * 8 + 2 * t] = m[nb][0];
+      sm[warp * C::HEADS + nb * 8 + 2 * t + 1] = m[nb][1];
+      sl[warp * C::HEADS + nb * 8 + 2 * t] = l[nb][0];
+      sl[warp * C::HEADS + nb * 8 + 2 * t + 1] = l[nb][1];
+    }
   }
 #pragma unroll
-  for (int nb = 0; nb < C::NB; ++nb) {
+  for (int mb = 0; mb < C::MB; ++mb) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = g + ((j >> 1) << 3);
-      so[(warp * kDecodeRows + r) * D + o_col<FP8>(nb, j, t)] = o[nb][j];
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int head = nb * 8 + 2 * t + (j & 1);
+        if (head < rows) so[(warp * C::HEADS + head) * D + o_dim<FP8>(mb, j, g)] = o[mb][nb][j];
+      }
     }
   }
   __syncthreads();
-  __shared__ float s_lse2[kDecodeRows];
-  if (threadIdx.x < kDecodeRows) {
+  __shared__ float s_lse2[C::HEADS];
+  if (threadIdx.x < C::HEADS) {
     const int r = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < C::WARPS; ++k) M = fmaxf(M, sm[k * kDecodeRows + r]);
+    for (int k = 0; k < C::WARPS; ++k) M = fmaxf(M, sm[k * C::HEADS + r]);
     float W = 0.f;
     float e[C::WARPS];
 #pragma unroll
     for (int k = 0; k < C::WARPS; ++k) {
-      e[k] = ex2(sm[k * kDecodeRows + r] - M);
-      W += e[k] * sl[k * kDecodeRows + r];
+      e[k] = ex2(sm[k * C::HEADS + r] - M);  // a warp without tiles has m = -inf: weight 0
+      W += e[k] * sl[k * C::HEADS + r];
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
 #pragma unroll
-    for (int k = 0; k < C::WARPS; ++k) sf[k * kDecodeRows + r] = e[k] * inv;
+    for (int k = 0; k < C::WARPS; ++k) sf[k * C::HEADS + r] = e[k] * inv;
     s_lse2[r] = M + __log2f(W);
   }
   __syncthreads();
@@ -344,7 +355,7 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
       const int r = idx / D, d = idx - r * D;
       float acc = 0.f;
 #pragma unroll
-      for (int k = 0; k < C::WARPS; ++k) acc += sf[k * kDecodeRows + r] * so[(k * kDecodeRows + r) * D + d];
+      for (int k = 0; k < C::WARPS; ++k) acc += sf[k * C::HEADS + r] * so[(k * C::HEADS + r) * D + d];
       out[idx] = __float2bfloat16_rn(acc * p.out_scale);
     }
     if (p.lse && threadIdx.x < rows)
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
       const int r = idx / D, d = idx - r * D;
       float acc = 0.f;
 #pragma unroll
-      for (int k = 0; k < C::WARPS; ++k) acc += sf[k * kDecodeRows + r] * so[(k * kDecodeRows + r) * D + d];
+      for (int k = 0; k < C::WARPS; ++k) acc += sf[k * C::HEADS + r] * so[(k * C::HEADS + r) * D + d];
       po[idx] = acc;
     }
     if (threadIdx.x < rows) p.part_lse[(int64_t)w.out_slot * kDecodeRows + threadIdx.x] = s_lse2[threadIdx.x];
@@ -365,34 +376,34 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
     __threadfence();
     __syncthreads();
     const int unit = p.slot_unit[w.out_slot];
-    const MergeItem m = p.merge[unit];
+    const MergeItem mi_ = p.merge[unit];
     if (threadIdx.x == 0) {
       const int done = atomicAdd(p.unit_count + unit, 1);
-      s_last = done == m.num_splits - 1;
+      s_last = done == mi_.num_splits - 1;
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    __shared__ float sM[kDecodeRows], sInv[kDecodeRows];
-    const float* lse = p.part_lse + (int64_t)m.first_slot * kDecodeRows;
+    __shared__ float sM[C::HEADS], sInv[C::HEADS];
+    const float* lse = p.part_lse + (int64_t)mi_.first_slot * kDecodeRows;
     if (threadIdx.x < rows) {
       const int r = threadIdx.x;
       float M = -INFINITY;
-      for (int s = 0; s < m.num_splits; ++s) M = fmaxf(M, __ldcg(lse + s * kDecodeRows + r));
+      for (int s = 0; s < mi_.num_splits; ++s) M = fmaxf(M, __ldcg(lse + s * kDecodeRows + r));
       float W = 0.f;
-      for (int s = 0; s < m.num_splits; ++s) W += ex2(__ldcg(lse + s * kDecodeRows + r) - M);
+      for (int s = 0; s < mi_.num_splits; ++s) W += ex2(__ldcg(lse + s * kDecodeRows + r) - M);
       sM[r] = M;
       sInv[r] = 1.f / W;
-      if (p.lse) p.lse[(int64_t)m.q_row * p.num_qo_heads + qh0 + r] = (M + __log2f(W)) * 0.69314718055994531f;
+      if (p.lse) p.lse[(int64_t)mi_.q_row * p.num_qo_heads + qh0 + r] = (M + __log2f(W)) * 0.69314718055994531f;
     }
     __syncthreads();
-    const float* pm = p.part_o + (int64_t)m.first_slot * kDecodeRows * D;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((int64_t)m.q_row * p.num_qo_heads + qh0) * D;
+    const float* pm = p.part_o + (int64_t)mi_.first_slot * kDecodeRows * D;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((int64_t)mi_.q_row * p.num_qo_heads + qh0) * D;
     for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
       const int r = idx / D;
       const float M = sM[r];
       float acc = 0.f;
-      for (int s = 0; s < m.num_splits; ++s)
+      for (int s = 0; s < mi_.num_splits; ++s)
         acc += ex2(__ldcg(lse + s * kDecodeRows + r) - M) * __ldcg(pm + (int64_t)s * kDecodeRows * D + idx);
       out[idx] = __float2bfloat16_rn(acc * sInv[r] * p.out_scale);
     }
@@ -400,30 +411,39 @@ __global__ void __launch_bounds__(128, 2) decode_kernel(const RunParams p, int32
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int NB>
 static cudaError_t launch_decode_t(const RunParams& p, cudaStream_t s) {
-  using C = DecodeCfg<D, FP8>;
+  using C = DecodeCfg<D, FP8, NB>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<D, FP8, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   int32_t* err = device_error_ptr();
   if (!err) return cudaErrorInvalidDevice;
-  decode_kernel<D, FP8><<<(unsigned)p.num_work, 128, C::SMEM, s>>>(p, err);
+  decode_kernel<D, FP8, NB><<<(unsigned)p.num_work, 128, C::SMEM, s>>>(p, err);
   return cudaGetLastError();
 }
 
+int decode_ctas_per_sm(int kv_dtype, int head_dim, int group) {
+  const bool nb2 = group > 8;
+  if (kv_dtype == PKV_FP8_E4M3) return nb2 ? DecodeCfg<128, true, 2>::CTAS : DecodeCfg<128, true, 1>::CTAS;
+  if (head_dim == 64) return nb2 ? DecodeCfg<64, false, 2>::CTAS : DecodeCfg<64, false, 1>::CTAS;
+  return nb2 ? DecodeCfg<128, false, 2>::CTAS : DecodeCfg<128, false, 1>::CTAS;
+}
+
 cudaError_t launch_decode(const RunParams& p, int kv_dtype, cudaStream_t s) {
+  const bool nb2 = p.group > 8;
   if (kv_dtype == PKV_FP8_E4M3) {
-    if (p.head_dim == 128) return launch_decode_t<128, true>(p, s);
-    return cudaErrorInvalidValue;
+    if (p.head_dim != 128) return cudaErrorInvalidValue;
+    return nb2 ? launch_decode_t<128, true, 2>(p, s) : launch_decode_t<128, true, 1>(p, s);
   }
-  if (p.head_dim == 128) return launch_decode_t<128, false>(p, s);
-  if (p.head_dim == 64) return launch_decode_t<64, false>(p, s);
+  if (p.head_dim == 128) return nb2 ? launch_decode_t<128, false, 2>(p, s) : launch_decode_t<128, false, 1>(p, s);
+  if (p.head_dim == 64) return nb2 ? launch_decode_t<64, false, 2>(p, s) : launch_decode_t<64, false, 1>(p, s);
   return cudaErrorInvalidValue;
 }
 

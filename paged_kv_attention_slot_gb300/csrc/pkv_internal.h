@@ -81,6 +81,7 @@ struct RunParams {
 cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, int64_t T, const pkv_cache& c,
                             float inv_k, float inv_v, cudaStream_t s);
 cudaError_t launch_decode(const RunParams& p, int kv_dtype, cudaStream_t s);
+int decode_ctas_per_sm(int kv_dtype, int head_dim, int group);  // resident decode CTAs per SM
 cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v,
                            int64_t total_tokens, cudaStream_t s);
 int prefill_supported(const char** why);
