@@ -178,6 +178,13 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   for (int i = 0; i < my_tiles; ++i) {
     cp_async_wait<C::STAGES - 2>();
     __syncwarp();
+    // refill the stage tile i-1 used (consumed in the previous iteration) before computing tile i,
+    // so STAGES-1 tiles stay in flight during the compute
+    {
+      const int nx = i + C::STAGES - 1;
+      if (nx < my_tiles) load_tile(nx, nx % C::STAGES);
+      cp_async_commit();
+    }
     const int stage = i % C::STAGES;
     const uint32_t kb = wsm_u + stage * 2 * C::TILE_B;
     const uint32_t vb = kb + C::TILE_B;
@@ -287,9 +294,6 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
       }
     }
     __syncwarp();
-    const int nx = i + C::STAGES - 1;
-    if (nx < my_tiles) load_tile(nx, nx % C::STAGES);
-    cp_async_commit();
   }
   cp_async_wait<0>();
 
