@@ -218,21 +218,36 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
       chunk = std::max<int64_t>(chunk, kDecodeMinChunk);
       chunk = align_up(chunk, kDecodeChunkAlign);
     }
-    P->kv_chunk = chunk;
-    // exact CTA count first, then fill in place
     // A unit is split only when it is clearly longer than the chunk: every split costs a partial
     // write and a merge, and units up to 1.25 chunks still balance under longest-first launch.
-    auto num_splits = [&](int64_t len) -> int64_t {
-      if (len <= chunk + chunk / 4) return 1;
-      return (len + chunk - 1) / chunk;
+    auto splits_for = [&](int64_t len, int64_t c) -> int64_t {
+      int64_t ns = len <= c + c / 4 ? 1 : (len + c - 1) / c;
+      if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
+      const int64_t piece = align_up((len + ns - 1) / ns, 16);
+      return (len + piece - 1) / piece;
     };
+    if (a->max_splits != 1) {
+      // Wave fit: CTAs longer than half a chunk cannot share a slot, so when there are more of them
+      // than resident slots (many equally long requests) a second wave would run a few of them
+      // alone.  Grow the chunk in 1/16 steps until they fit one wave.
+      const int64_t slots = (int64_t)sms * pkv::decode_ctas_per_sm(a->kv_dtype, a->head_dim, G) * kDecodeWaves;
+      auto long_items = [&](int64_t c) -> int64_t {
+        int64_t n = 0;
+        for (const Unit& u : units) {
+          const int64_t len = u.hi - u.lo, ns = splits_for(len, c);
+          if (2 * ((len + ns - 1) / ns) > c) n += ns;
+        }
+        return n * a->num_kv_heads * groups;
+      };
+      int64_t c = chunk;
+      for (int it = 0; it < 16 && long_items(c) > slots; ++it) c = align_up(c + c / 16, kDecodeChunkAlign);
+      if (long_items(c) <= slots) chunk = c;
+    }
+    P->kv_chunk = chunk;
+    auto num_splits = [&](int64_t len) -> int64_t { return splits_for(len, chunk); };
     int64_t items = 0, merges = 0;
     for (const Unit& u : units) {
-      const int64_t len = u.hi - u.lo;
-      int64_t ns = num_splits(len);
-      if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
-      const int64_t c = align_up((len + ns - 1) / ns, 16);
-      ns = (len + c - 1) / c;
+      const int64_t ns = num_splits(u.hi - u.lo);
       items += ns;
       merges += ns > 1;
     }
@@ -244,10 +259,8 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     int64_t slot = 0;
     for (const Unit& u : units) {
       const int64_t len = u.hi - u.lo;
-      int64_t ns = num_splits(len);
-      if (a->max_splits > 1) ns = std::min<int64_t>(ns, a->max_splits);
+      const int64_t ns = num_splits(len);
       const int64_t c = align_up((len + ns - 1) / ns, 16);
-      ns = (len + c - 1) / c;
       const int32_t q_row = P->req[u.req].q_begin;
       for (int32_t h = 0; h < a->num_kv_heads; ++h) {
         for (int32_t g = 0; g < groups; ++g) {

@@ -122,27 +122,49 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   constexpr int RPI = 32 / C::CH;  // rows per warp instruction
   const int lc = lane % C::CH;
   const int lsub = lane / C::CH;
+  const int ps = p.page_size;
+  const int ps_shift = (ps & (ps - 1)) == 0 ? __ffs(ps) - 1 : -1;  // page sizes are usually powers of 2
+  auto page_of = [&](int key) -> int { return ps_shift >= 0 ? key >> ps_shift : key / ps; };
+  const int64_t row_step = (int64_t)RPI * p.stride_token_b;  // bytes between the rows of consecutive instructions
   // The page id of the row this lane resolves is fetched one tile ahead (this warp's next tile is
   // 4 tiles = 64 keys further), so the index load never stalls the issue of the copies.
   auto fetch_page = [&](int key) -> int {
-    return key < w.kv_end ? __ldg(p.kv_indices + ri.page_base + key / p.page_size) : 0;
+    return key < w.kv_end ? __ldg(p.kv_indices + ri.page_base + page_of(key)) : 0;
   };
   int next_page = fetch_page(w.kv_begin + warp * C::KEYS + lr);
   auto load_tile = [&](int i, int stage) {
-    const int key = w.kv_begin + (warp + i * C::WARPS) * C::KEYS + lr;
+    const int key0 = w.kv_begin + (warp + i * C::WARPS) * C::KEYS;
+    const int key = key0 + lr;
     const int page = next_page;
     next_page = fetch_page(key + C::WARPS * C::KEYS);
+    const uint32_t dk = wsm_u + stage * 2 * C::TILE_B;
+    const uint32_t dv = dk + C::TILE_B;
+    // Common case: all 16 keys present and on one page (page size >= 16, chunk starts aligned), so
+    // every lane has the same page id and the row addresses follow from one base and a stride.
+    const bool one_page = key0 + C::KEYS <= w.kv_end && page_of(key0) == page_of(key0 + C::KEYS - 1) &&
+                          (unsigned long long)(unsigned)page < (unsigned long long)p.num_pages;
+    if (__all_sync(0xffffffffu, one_page)) {
+      const int off0 = key0 - page_of(key0) * ps;
+      const int64_t base = (int64_t)page * p.stride_page_b + (int64_t)(off0 + lsub) * p.stride_token_b + head_off + lc * 16;
+      const char* ks = p.k_pool + base;
+      const char* vs = p.v_pool + base;
+#pragma unroll
+      for (int j = 0; j < C::KEYS / RPI; ++j) {
+        const int row = j * RPI + lsub;
+        const uint32_t sw = row * C::ROWB + ((lc ^ (row & 7)) << 4);
+        cp_async16(dk + sw, ks + j * row_step, 16u);
+        cp_async16(dv + sw, vs + j * row_step, 16u);
+      }
+      return;
+    }
     int64_t roff = -1;
     if (key < w.kv_end) {
-      const int lp = key / p.page_size;
-      const int off = key - lp * p.page_size;
+      const int off = key - page_of(key) * ps;
       if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages)
         record_error(err, PKV_DEVERR_PAGE_RANGE);
       else
         roff = (int64_t)page * p.stride_page_b + (int64_t)off * p.stride_token_b + head_off;
     }
-    const uint32_t dk = wsm_u + stage * 2 * C::TILE_B;
-    const uint32_t dv = dk + C::TILE_B;
 #pragma unroll
     for (int j = 0; j < C::KEYS / RPI; ++j) {
       const int row = j * RPI + lsub;
@@ -154,7 +176,7 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     }
   };
 
-  float m[NB][2], l[NB][2];  // per head column 2t, 2t+1: running max (log2 units) and this lane's sum
+  float m[NB][2], l[NB][2];  // per head column 2t, 2t+1: reference max (log2 units) and this lane's sum
   float o[C::MB][NB][4];     // O^T: rows = head dims, columns = heads
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
@@ -175,6 +197,7 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   const int k_key = ((mi & 1) << 3) + rr;  // matrices: (keys 0-7, c), (keys 8-15, c), (keys 0-7, c+1), (8-15, c+1)
   const int v_key = ((mi >> 1) << 3) + rr; // matrices: (keys 0-7, c), (keys 0-7, c+1), (keys 8-15, c), (8-15, c+1)
 
+  int stage = 0, fill = C::STAGES - 1;  // ring slot of tile i and of tile i + STAGES - 1
   for (int i = 0; i < my_tiles; ++i) {
     cp_async_wait<C::STAGES - 2>();
     __syncwarp();
@@ -182,12 +205,13 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     // so STAGES-1 tiles stay in flight during the compute
     {
       const int nx = i + C::STAGES - 1;
-      if (nx < my_tiles) load_tile(nx, nx % C::STAGES);
+      if (nx < my_tiles) load_tile(nx, fill);
       cp_async_commit();
+      fill = fill + 1 == C::STAGES ? 0 : fill + 1;
     }
-    const int stage = i % C::STAGES;
     const uint32_t kb = wsm_u + stage * 2 * C::TILE_B;
     const uint32_t vb = kb + C::TILE_B;
+    stage = stage + 1 == C::STAGES ? 0 : stage + 1;
     const int key0 = w.kv_begin + (warp + i * C::WARPS) * C::KEYS;
 
     // ---- S^T = K Q^T for 16 keys ----
@@ -209,11 +233,13 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
         uint32_t r[4];
         const int chunk = c + (mi >> 1);
         ldsm_x4(r, kb + k_key * C::ROWB + ((chunk ^ (k_key & 7)) << 4));
-        // r[0]: keys 0-7 / chunk c, r[1]: keys 8-15 / chunk c, r[2], r[3]: chunk c + 1
+        // r[0]: keys 0-7 / chunk c, r[1]: keys 8-15 / chunk c, r[2], r[3]: chunk c + 1; the low
+        // code pair of each register feeds k-step c + h's first half, the high pair its second
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t a[4] = {e4m3x2_to_f16x2(r[2 * h] & 0xffffu), e4m3x2_to_f16x2(r[2 * h + 1] & 0xffffu),
-                                 e4m3x2_to_f16x2(r[2 * h] >> 16), e4m3x2_to_f16x2(r[2 * h + 1] >> 16)};
+          uint32_t a[4];
+          e4m3x4_to_f16x2x2(r[2 * h], a[0], a[2]);
+          e4m3x4_to_f16x2x2(r[2 * h + 1], a[1], a[3]);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) mma_f16(s[nb], a, qb[c + h][nb][0], qb[c + h][nb][1]);
         }
@@ -221,38 +247,51 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     }
 
     // ---- online softmax per head column (log2 domain) ----
-    const bool lo_ok = key0 + g < w.kv_end, hi_ok = key0 + g + 8 < w.kv_end;
+    // The reference max m moves only when a column's tile max exceeds it by more than 2^8 (one
+    // warp-wide decision), so most tiles skip the O rescale; probabilities stay below 2^8.
+    const bool full = key0 + C::KEYS <= w.kv_end;
     uint32_t pb[NB][2];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-      float x0 = lo_ok ? s[nb][0] * p.scale_log2 : -INFINITY;  // key g,     head 2t
-      float x1 = lo_ok ? s[nb][1] * p.scale_log2 : -INFINITY;  // key g,     head 2t+1
-      float x2 = hi_ok ? s[nb][2] * p.scale_log2 : -INFINITY;  // key g + 8, head 2t
-      float x3 = hi_ok ? s[nb][3] * p.scale_log2 : -INFINITY;  // key g + 8, head 2t+1
+      float x0 = s[nb][0] * p.scale_log2;  // key g,     head 2t
+      float x1 = s[nb][1] * p.scale_log2;  // key g,     head 2t+1
+      float x2 = s[nb][2] * p.scale_log2;  // key g + 8, head 2t
+      float x3 = s[nb][3] * p.scale_log2;  // key g + 8, head 2t+1
+      if (!full) {
+        const bool lo_ok = key0 + g < w.kv_end, hi_ok = key0 + g + 8 < w.kv_end;
+        x0 = lo_ok ? x0 : -INFINITY;
+        x1 = lo_ok ? x1 : -INFINITY;
+        x2 = hi_ok ? x2 : -INFINITY;
+        x3 = hi_ok ? x3 : -INFINITY;
+      }
       float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
       for (int sh = 4; sh < 32; sh <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
       }
-      // every tile holds at least one visible key, so the new maxima are finite
-      const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
-      const float c0 = ex2(m[nb][0] - mn0), c1 = ex2(m[nb][1] - mn1);
-      m[nb][0] = mn0;
-      m[nb][1] = mn1;
-      x0 = ex2(x0 - mn0);
-      x1 = ex2(x1 - mn1);
-      x2 = ex2(x2 - mn0);
-      x3 = ex2(x3 - mn1);
-      l[nb][0] = l[nb][0] * c0 + (x0 + x2);
-      l[nb][1] = l[nb][1] * c1 + (x1 + x3);
+      // every tile holds at least one visible key, so the tile maxima are finite
+      if (__any_sync(0xffffffffu, mx0 > m[nb][0] + 8.f || mx1 > m[nb][1] + 8.f)) {
+        const float mn0 = fmaxf(m[nb][0], mx0), mn1 = fmaxf(m[nb][1], mx1);
+        const float c0 = ex2(m[nb][0] - mn0), c1 = ex2(m[nb][1] - mn1);
+        m[nb][0] = mn0;
+        m[nb][1] = mn1;
+        l[nb][0] *= c0;
+        l[nb][1] *= c1;
 #pragma unroll
-      for (int mb = 0; mb < C::MB; ++mb) {
-        o[mb][nb][0] *= c0;
-        o[mb][nb][1] *= c1;
-        o[mb][nb][2] *= c0;
-        o[mb][nb][3] *= c1;
+        for (int mb = 0; mb < C::MB; ++mb) {
+          o[mb][nb][0] *= c0;
+          o[mb][nb][1] *= c1;
+          o[mb][nb][2] *= c0;
+          o[mb][nb][3] *= c1;
+        }
       }
+      x0 = ex2(x0 - m[nb][0]);
+      x1 = ex2(x1 - m[nb][1]);
+      x2 = ex2(x2 - m[nb][0]);
+      x3 = ex2(x3 - m[nb][1]);
+      l[nb][0] += x0 + x2;
+      l[nb][1] += x1 + x3;
       // P^T in accumulator layout (row = key, column pair = heads) -> B operand (k = keys, n = head)
       if constexpr (!FP8) {
         pb[nb][0] = movmatrix_trans(pack_bf16(x0, x1));
@@ -282,14 +321,15 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
         // r[0]: keys 0-7 x chunk c, r[1]: keys 0-7 x chunk c+1, r[2]: keys 8-15 x chunk c,
         // r[3]: keys 8-15 x chunk c+1.  Each register holds, for byte-pair column g:
         // (key 2t: d, d+1), (key 2t+1: d, d+1) with d = 16 chunk + 2g; bytes 0/2 are the even dim,
-        // bytes 1/3 the odd one.
+        // bytes 1/3 the odd one.  One byte permute puts the even pair in the low half and the odd
+        // pair in the high half.
+        uint32_t ev[4], od[4];
 #pragma unroll
-        for (int par = 0; par < 2; ++par) {
-          const uint32_t sel = par ? 0x0031u : 0x0020u;
-          const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(r[0], 0, sel)), e4m3x2_to_f16x2(__byte_perm(r[1], 0, sel)),
-                                 e4m3x2_to_f16x2(__byte_perm(r[2], 0, sel)), e4m3x2_to_f16x2(__byte_perm(r[3], 0, sel))};
+        for (int k = 0; k < 4; ++k) e4m3x4_to_f16x2x2(__byte_perm(r[k], 0, 0x3120u), ev[k], od[k]);
 #pragma unroll
-          for (int nb = 0; nb < NB; ++nb) mma_f16(o[c + par][nb], a, pb[nb][0], pb[nb][1]);
+        for (int nb = 0; nb < NB; ++nb) {
+          mma_f16(o[c][nb], ev, pb[nb][0], pb[nb][1]);
+          mma_f16(o[c + 1][nb], od, pb[nb][0], pb[nb][1]);
         }
       }
     }
@@ -388,29 +428,113 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    __shared__ float sM[C::HEADS], sInv[C::HEADS];
-    const float* lse = p.part_lse + (int64_t)mi_.first_slot * kDecodeRows;
-    if (threadIdx.x < rows) {
-      const int r = threadIdx.x;
-      float M = -INFINITY;
-      for (int s = 0; s < mi_.num_splits; ++s) M = fmaxf(M, __ldcg(lse + s * kDecodeRows + r));
-      float W = 0.f;
-      for (int s = 0; s < mi_.num_splits; ++s) W += ex2(__ldcg(lse + s * kDecodeRows + r) - M);
-      sM[r] = M;
-      sInv[r] = 1.f / W;
-      if (p.lse) p.lse[(int64_t)mi_.q_row * p.num_qo_heads + qh0 + r] = (M + __log2f(W)) * 0.69314718055994531f;
+    // Online merge over chunks of splits: the chunk's log2-sum-exps are staged in shared memory by
+    // all threads and turned into per-row weights 2^(lse_s - M) once; each thread owns float4 columns
+    // of the output and reads 8 partials per round, so 8 L2 reads per column are in flight.
+    constexpr int V4 = C::HEADS * D / 4;            // float4s of the (at most HEADS) output rows
+    constexpr int PER_T = (V4 + 127) / 128;         // float4s per thread
+    constexpr int SLOT4 = kDecodeRows * D / 4;      // float4s between consecutive partials
+    const int n4 = rows * D / 4;
+    const int cap = C::SMEM / (4 * C::HEADS) - 2;   // splits per chunk that fit the shared scratch
+    float* wgt = reinterpret_cast<float*>(smem);    // [cap][HEADS] lse, then weights
+    __shared__ float sM[C::HEADS], sScale[C::HEADS], sW[C::HEADS];
+    if (threadIdx.x < C::HEADS) {
+      sM[threadIdx.x] = -INFINITY;
+      sW[threadIdx.x] = 0.f;
     }
-    __syncthreads();
-    const float* pm = p.part_o + (int64_t)mi_.first_slot * kDecodeRows * D;
+    float4 acc[PER_T];
+    int col[PER_T], crow[PER_T];
+#pragma unroll
+    for (int k = 0; k < PER_T; ++k) {
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      col[k] = threadIdx.x + k * 128;
+      crow[k] = col[k] * 4 / D;
+    }
+    const float* lse_g = p.part_lse + (int64_t)mi_.first_slot * kDecodeRows;
+    const float4* pm = reinterpret_cast<const float4*>(p.part_o + (int64_t)mi_.first_slot * kDecodeRows * D);
+    for (int s0 = 0; s0 < mi_.num_splits; s0 += cap) {
+      const int ns = min(cap, mi_.num_splits - s0);
+      __syncthreads();
+      for (int e = threadIdx.x; e < ns * C::HEADS; e += blockDim.x) {
+        const int sp = e / C::HEADS, r = e - sp * C::HEADS;
+        wgt[e] = r < rows ? __ldcg(lse_g + (int64_t)(s0 + sp) * kDecodeRows + r) : -INFINITY;
+      }
+      __syncthreads();
+      if (threadIdx.x < rows) {
+        const int r = threadIdx.x;
+        float Mc = sM[r];
+        for (int sp = 0; sp < ns; ++sp) Mc = fmaxf(Mc, wgt[sp * C::HEADS + r]);
+        const bool none = Mc == -INFINITY;            // no key seen yet: keep every weight 0
+        const float sc = none ? 1.f : ex2(sM[r] - Mc);  // 0 on the first chunk
+        float W = sW[r] * sc;
+        for (int sp = 0; sp < ns; ++sp) {
+          const float e = none ? 0.f : ex2(wgt[sp * C::HEADS + r] - Mc);
+          wgt[sp * C::HEADS + r] = e;
+          W += e;
+        }
+        sM[r] = Mc;
+        sW[r] = W;
+        sScale[r] = sc;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < PER_T; ++k) {
+        if (col[k] < n4) {
+          const float sc = sScale[crow[k]];
+          acc[k].x *= sc;
+          acc[k].y *= sc;
+          acc[k].z *= sc;
+          acc[k].w *= sc;
+        }
+      }
+      const float4* base = pm + (int64_t)s0 * SLOT4;
+      int sp = 0;
+      for (; sp + 8 <= ns; sp += 8) {
+        float4 x[8][PER_T];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int k = 0; k < PER_T; ++k)
+            x[u][k] = col[k] < n4 ? __ldcg(base + (int64_t)(sp + u) * SLOT4 + col[k]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int k = 0; k < PER_T; ++k) {
+            const float wv = wgt[(sp + u) * C::HEADS + (col[k] < n4 ? crow[k] : 0)];
+            acc[k].x += wv * x[u][k].x;
+            acc[k].y += wv * x[u][k].y;
+            acc[k].z += wv * x[u][k].z;
+            acc[k].w += wv * x[u][k].w;
+          }
+      }
+      for (; sp < ns; ++sp) {
+#pragma unroll
+        for (int k = 0; k < PER_T; ++k) {
+          if (col[k] < n4) {
+            const float4 x = __ldcg(base + (int64_t)sp * SLOT4 + col[k]);
+            const float wv = wgt[sp * C::HEADS + crow[k]];
+            acc[k].x += wv * x.x;
+            acc[k].y += wv * x.y;
+            acc[k].z += wv * x.z;
+            acc[k].w += wv * x.w;
+          }
+        }
+      }
+    }
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((int64_t)mi_.q_row * p.num_qo_heads + qh0) * D;
-    for (int idx = threadIdx.x; idx < rows * D; idx += blockDim.x) {
-      const int r = idx / D;
-      const float M = sM[r];
-      float acc = 0.f;
-      for (int s = 0; s < mi_.num_splits; ++s)
-        acc += ex2(__ldcg(lse + s * kDecodeRows + r) - M) * __ldcg(pm + (int64_t)s * kDecodeRows * D + idx);
-      out[idx] = __float2bfloat16_rn(acc * sInv[r] * p.out_scale);
+#pragma unroll
+    for (int k = 0; k < PER_T; ++k) {
+      if (col[k] < n4) {
+        const float W = sW[crow[k]];
+        const float f = W > 0.f ? p.out_scale / W : 0.f;
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + col[k] * 4);
+        o2[0] = __floats2bfloat162_rn(acc[k].x * f, acc[k].y * f);
+        o2[1] = __floats2bfloat162_rn(acc[k].z * f, acc[k].w * f);
+      }
     }
+    if (p.lse && threadIdx.x < rows)
+      p.lse[(int64_t)mi_.q_row * p.num_qo_heads + qh0 + threadIdx.x] =
+          (sM[threadIdx.x] + __log2f(sW[threadIdx.x])) * 0.69314718055994531f;
     if (threadIdx.x == 0) p.unit_count[unit] = 0;  // ready for the next run of this plan
   }
 }

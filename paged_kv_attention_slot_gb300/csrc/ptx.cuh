@@ -82,6 +82,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(r) : "r"(two_codes));
   return r;
 }
+// four E4M3 codes to two f16x2: bytes 0,1 -> lo, bytes 2,3 -> hi (the register halves feed the
+// conversions directly)
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_codes));
+}
 // two floats to two E4M3 codes, round to nearest even, saturate to finite; lo -> low byte
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   uint32_t r;
