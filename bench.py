@@ -259,9 +259,19 @@ def _device_state(b, device):
     import paged_kv_attention_slot_gb300 as pk
 
     st = {}
-    st["k_pool"] = b.k_pool.to(device)
-    st["v_pool"] = b.v_pool.to(device)
-    st["cache"] = pk.KVCache(st["k_pool"], st["v_pool"])
+    if b.kv_dtype == "bf16":
+        st["k_pool"] = b.k_pool.to(device)
+        st["v_pool"] = b.v_pool.to(device)
+        st["cache"] = pk.KVCache(st["k_pool"], st["v_pool"])
+    else:  # FP8 pools written by the library's own quantising kv_store
+        P, ps, H, D = b.k_pool.shape
+        st["k_pool"] = torch.zeros((P, ps, H, D), dtype=torch.uint8, device=device)
+        st["v_pool"] = torch.zeros((P, ps, H, D), dtype=torch.uint8, device=device)
+        st["cache"] = pk.KVCache(st["k_pool"], st["v_pool"], b.k_scale, b.v_scale)
+        slots = torch.arange(P * ps, dtype=torch.int64, device=device)
+        pk.kv_store(b.k_pool.to(device).view(P * ps, H, D), b.v_pool.to(device).view(P * ps, H, D), slots,
+                    st["cache"])
+        torch.cuda.synchronize()
     st["q"] = b.q.to(device)
     st["k_new"] = b.k_new.to(device)
     st["v_new"] = b.v_new.to(device)
@@ -318,6 +328,50 @@ def run_steps(b, st, plan, steps, warmup, dist_on, record_run_events=True):
     return total_ms, run_ms
 
 
+def kernel_ms(run_once, reps=20, iters=7):
+    """Average device time of one run launch: `reps` launches captured in one CUDA graph and replayed
+    between two CUDA events on the launching stream (no host launch gaps between the kernels).  Falls
+    back to eager back-to-back launches if capture fails."""
+    import torch
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            run_once()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    mode = f"CUDA graph of {reps} launches, replayed"
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(reps):
+                run_once()
+
+        def replay():
+            graph.replay()
+    except Exception as e:  # capture unsupported here: time eager launches instead
+        torch.cuda.synchronize()
+        mode = f"{reps} eager back-to-back launches (graph capture failed: {type(e).__name__})"
+
+        def replay():
+            for _ in range(reps):
+                run_once()
+    stream = torch.cuda.current_stream()
+    replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    per = []
+    for _ in range(iters):
+        e0.record(stream)
+        replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) / reps)
+    return statistics.median(per), mode
+
+
 def run_e2e(b, st, plan, steps, warmup):
     """Same step through the public API from pinned HOST buffers: H2D of the step's inputs, D2H of O."""
     import torch
@@ -356,6 +410,32 @@ def run_e2e(b, st, plan, steps, warmup):
     return dt, h2d, d2h
 
 
+def decode_other_configs(device, hbm):
+    """Decode kernel time on the other decode workloads (same kernel, CUDA-graph replay timing)."""
+    import torch
+
+    import paged_kv_attention_slot_gb300 as pk
+    import workloads as W
+
+    res = []
+    for n, window, name in ((4, -1, "llama70b_ragged_decode: batch 256, 64 q / 8 kv, log-normal KV (median 1024), page 64, bf16"),
+                            (5, -1, "fp8_long_decode: batch 2, KV 131072, 32 q / 8 kv, page 128, FP8 E4M3 KV"),
+                            (5, 4096, "fp8_long_decode_window: as above, sliding window 4096")):
+        b = W.workload(n, window_left=window)
+        st = _device_state(b, device)
+        plan = pk.Plan()
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **_plan_kw(b))
+        info = plan.info()
+        k_ms, mode = kernel_ms(lambda: plan.run(st["q"], st["cache"], out=st["out"]))
+        gbs = b.kv_bytes_read() / (k_ms * 1e-3) / 1e9
+        res.append({"workload": name, "kv_bytes": b.kv_bytes_read(), "kernel_ms": round(k_ms, 4),
+                    "achieved": round(gbs, 2), "unit": "GB/s", "frac": round(gbs / hbm, 4), "timing": mode,
+                    "plan": {"ctas": info["num_work"], "merge_units": info["num_merge"], "kv_chunk": info["kv_chunk"]}})
+        del st, plan
+        torch.cuda.empty_cache()
+    return res
+
+
 def prefill_measure(device, steps, warmup, peak_tflops):
     """Prefix-cached extend (page size 1): plan + KV write + prefill per step, TFLOP/s."""
     import numpy as np
@@ -378,7 +458,8 @@ def prefill_measure(device, steps, warmup, peak_tflops):
     flops = 4.0 * b.head_dim * b.num_qo_heads * pairs
     total_ms, run_ms = run_steps(b, st, plan, steps, warmup, False)
     run_avg = statistics.mean(run_ms)
-    achieved = flops / (run_avg * 1e-3) / 1e12
+    k_ms, k_mode = kernel_ms(lambda: plan.run(st["q"], st["cache"], out=st["out"]), reps=10, iters=5)
+    achieved = flops / (k_ms * 1e-3) / 1e12
     return {
         "workload": "prefix_extend: batch 8, new U[128,2048], prefix U[0,4096], page 1, 32q/8kv, D 128, bf16",
         "metric": "prefill TFLOP/s (causally visible pairs)",
@@ -387,9 +468,9 @@ def prefill_measure(device, steps, warmup, peak_tflops):
         "ms_per_step": round(total_ms / steps, 4),
         "flops_per_step": flops,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tflops, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak_tflops, 4),
+                     "frac": round(achieved / peak_tflops, 4), "kernel_ms": round(k_ms, 4), "timing": k_mode,
                      "traffic": _traffic("prefill", ["prefill.cu", "ptx.cuh", "tc.cuh"])},
-        "run_ms_mean": round(run_avg, 4),
+        "run_ms_mean_in_steps": round(run_avg, 4),
         "gpu_launches_per_step": 2,
     }
 
@@ -403,6 +484,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--only-prefill", action="store_true", help="measure the prefill workload alone (profiling)")
+    ap.add_argument("--no-other-decode", action="store_true", help="skip the other decode workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -461,12 +543,16 @@ def main():
     err = pk.device_error()
 
     run_avg = statistics.mean(run_ms)
-    achieved = kv_bytes / (run_avg * 1e-3) / 1e9
+    k_ms, k_mode = kernel_ms(lambda: plan.run(st["q"], st["cache"], out=st["out"]))
+    achieved = kv_bytes / (k_ms * 1e-3) / 1e9
     launches_per_step = 2  # kv_store + decode (the split-KV merge runs inside the decode kernel)
 
     prefill = None
     if not args.no_prefill and rank == 0:
         prefill = prefill_measure(device, max(5, args.steps // 2), 3, tf_burst)
+    other = None
+    if not args.no_other_decode and rank == 0:
+        other = decode_other_configs(device, hbm)
 
     cpu = None
     if pool is not None:
@@ -499,13 +585,16 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src,
                          "kernel": "decode_kernel (split-KV merge fused), one launch per decode_run",
+                         "kernel_ms": round(k_ms, 4), "timing": k_mode,
+                         "run_ms_mean_in_steps": round(run_avg, 4),
                          "traffic": _traffic("decode", ["decode.cu", "ptx.cuh"])},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
             "prefill": prefill,
-            "device_error": err,
+            "decode_other_configs": other,
+            "device_error": pk.device_error() if err == 0 else err,
         }
         print(json.dumps(line))
     if dist_on:

@@ -273,7 +273,11 @@ int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info);
 
 /* Copy the plan's work list to host memory: 8 int32 per CTA, in launch order:
  *   {request, kv_head, head_group, kv_begin, kv_end, q_row, out_slot, q_rows}
- * (out_slot = partial slot or -1 when the CTA writes the final output).  `capacity` is in int32. */
+ * (out_slot = partial slot or -1 when the CTA writes the final output).  A decode CTA with
+ * out_slot = -1 reads all of [kv_begin, kv_end); the CTAs with consecutive partial slots of one
+ * (request, kv_head, head_group) share the same [kv_begin, kv_end) and divide its 64-key groups
+ * among themselves at run time (each warp starts on its own group, then takes the next unclaimed
+ * one from a counter in the workspace).  `capacity` is in int32. */
 int pkv_plan_work_items(const pkv_plan* plan, int32_t* out, int64_t capacity);
 
 /* ---------------------------------------------------------------------------------------------- */

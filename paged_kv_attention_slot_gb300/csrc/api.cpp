@@ -75,13 +75,18 @@ int query_num_sms(int32_t requested, int32_t* out) {
   return PKV_OK;
 }
 
-// Order the work list longest first (stable counting sort on the key length, bucketed so that at
-// most 4096 buckets are used: the order is exact up to 1/4096 of the longest key range).
+// Keys one CTA of the item is expected to read: its range, shared by num_splits CTAs.
+inline int32_t item_share(const WorkItem& x) {
+  return (x.kv_end - x.kv_begin + x.num_splits - 1) / x.num_splits;
+}
+
+// Order the work list longest first (stable counting sort on the per-CTA share, bucketed so that
+// at most 4096 buckets are used: the order is exact up to 1/4096 of the longest share).
 void order_longest_first(std::vector<WorkItem>& w) {
   const size_t n = w.size();
   if (n < 2) return;
   int32_t maxlen = 0;
-  for (const WorkItem& x : w) maxlen = std::max(maxlen, x.kv_end - x.kv_begin);
+  for (const WorkItem& x : w) maxlen = std::max(maxlen, item_share(x));
   int shift = 0;
   while ((maxlen >> shift) >= 4096) ++shift;
   const int nb = (maxlen >> shift) + 1;
@@ -91,10 +96,10 @@ void order_longest_first(std::vector<WorkItem>& w) {
   tmp.resize(n);
   uint32_t* c = count.data();
   const WorkItem* src = w.data();
-  for (size_t i = 0; i < n; ++i) ++c[nb - ((src[i].kv_end - src[i].kv_begin) >> shift)];
+  for (size_t i = 0; i < n; ++i) ++c[nb - (item_share(src[i]) >> shift)];
   for (int d = 0; d < nb; ++d) c[d + 1] += c[d];
   WorkItem* dst = tmp.data();
-  for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - ((src[i].kv_end - src[i].kv_begin) >> shift)]++] = src[i];
+  for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - (item_share(src[i]) >> shift)]++] = src[i];
   w.swap(tmp);
 }
 
@@ -188,7 +193,6 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   P->total_tokens = total_tokens;
   P->work.clear();
   P->merge.clear();
-  P->slot_unit.clear();
   P->num_partials = 0;
   P->kv_tokens = 0;
   P->kv_chunk = 0;
@@ -257,23 +261,29 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     WorkItem* wi = P->work.data();
     MergeItem* mi = P->merge.data();
     int64_t slot = 0;
+    // The ns CTAs of a split unit all draw from the unit's whole key range: each warp starts on a
+    // 64-key group of its own and then claims further groups from a per-unit counter at run time,
+    // so CTAs on faster SMs read more and all of them finish together.
     for (const Unit& u : units) {
-      const int64_t len = u.hi - u.lo;
-      const int64_t ns = num_splits(len);
-      const int64_t c = align_up((len + ns - 1) / ns, 16);
+      const int64_t ns = num_splits(u.hi - u.lo);
       const int32_t q_row = P->req[u.req].q_begin;
       for (int32_t h = 0; h < a->num_kv_heads; ++h) {
         for (int32_t g = 0; g < groups; ++g) {
+          const int32_t unit = ns > 1 ? (int32_t)(mi - P->merge.data()) : -1;
           for (int64_t s = 0; s < ns; ++s) {
             WorkItem& w = *wi++;
             w.req = u.req;
             w.kv_head = h;
             w.head_group = g;
-            w.kv_begin = (int32_t)(u.lo + s * c);
-            w.kv_end = (int32_t)std::min<int64_t>(u.hi, u.lo + (s + 1) * c);
+            w.kv_begin = u.lo;
+            w.kv_end = u.hi;
             w.q_row = q_row;
             w.out_slot = ns > 1 ? (int32_t)(slot + s) : -1;
             w.q_rows = 1;
+            w.page_base = P->req[u.req].page_base;
+            w.split = (int32_t)s;
+            w.num_splits = (int32_t)ns;
+            w.unit = unit;
           }
           if (ns > 1) {
             MergeItem& m = *mi++;
@@ -289,9 +299,6 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
       }
     }
     P->num_partials = slot;
-    P->slot_unit.resize((size_t)slot);
-    for (size_t u = 0; u < P->merge.size(); ++u)
-      for (int32_t k = 0; k < P->merge[u].num_splits; ++k) P->slot_unit[P->merge[u].first_slot + k] = (int32_t)u;
   } else {
     const int32_t tok_per_tile = kPrefillTiles * (kPrefillRows / G);  // tokens per CTA
     for (int32_t i = 0; i < B; ++i) {
@@ -312,6 +319,10 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
           w.q_row = r.q_begin + t0;
           w.out_slot = -1;
           w.q_rows = rows;
+          w.page_base = r.page_base;
+          w.split = 0;
+          w.num_splits = 1;
+          w.unit = -1;
           P->work.push_back(w);
         }
       }
@@ -331,10 +342,10 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   off = align_up(off + P->req.size() * sizeof(ReqInfo), 256);
   P->off_idx = off;
   off = align_up(off + P->indices.size() * sizeof(int32_t), 256);
-  P->off_slot_unit = off;
-  off = align_up(off + P->slot_unit.size() * sizeof(int32_t), 256);
-  P->off_count = off;  // zero-filled by the metadata copy; the kernel leaves it zero after each run
+  P->off_count = off;  // [unit_count | claim lines], zero-filled by the metadata copy; zero again after each run
   off = align_up(off + P->merge.size() * sizeof(int32_t), 256);
+  P->off_claim = off;
+  off = align_up(off + P->merge.size() * pkv::kClaimStride * sizeof(int32_t), 256);
   P->meta_bytes = off;
   P->off_plse = off;
   off = align_up(off + (size_t)P->num_partials * pkv::kDecodeRows * sizeof(float), 256);
@@ -376,8 +387,8 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
   p.kv_indices = (const int32_t*)(ws + P->off_idx);
   p.part_lse = (float*)(ws + P->off_plse);
   p.part_o = (float*)(ws + P->off_po);
-  p.slot_unit = (const int32_t*)(ws + P->off_slot_unit);
   p.unit_count = (int32_t*)(ws + P->off_count);
+  p.claim = (int32_t*)(ws + P->off_claim);
   p.q = q;
   p.o = o;
   p.lse = lse;
@@ -518,7 +529,6 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
   std::memcpy(h + plan->off_merge, plan->merge.data(), plan->merge.size() * sizeof(MergeItem));
   std::memcpy(h + plan->off_req, plan->req.data(), plan->req.size() * sizeof(ReqInfo));
   std::memcpy(h + plan->off_idx, plan->indices.data(), plan->indices.size() * sizeof(int32_t));
-  std::memcpy(h + plan->off_slot_unit, plan->slot_unit.data(), plan->slot_unit.size() * sizeof(int32_t));
   cudaStream_t s = (cudaStream_t)stream;
   PKV_CUDA(cudaMemcpyAsync(workspace, h, plan->meta_bytes, cudaMemcpyHostToDevice, s), "plan metadata copy");
   PKV_CUDA(cudaEventRecord(plan->copy_done, s), "cudaEventRecord");
@@ -640,9 +650,10 @@ int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info) {
 int pkv_plan_work_items(const pkv_plan* plan, int32_t* out, int64_t capacity) {
   if (!plan || !out) return fail(PKV_EINVAL, "NULL argument");
   if (!plan->valid) return fail(PKV_EINVAL, "plan has not been planned");
-  const int64_t need = (int64_t)plan->work.size() * 8;
+  const int64_t need = (int64_t)plan->work.size() * pkv::kWorkItemPublicFields;
   if (capacity < need) return fail(PKV_EINVAL, "capacity too small: need " + std::to_string(need));
-  std::memcpy(out, plan->work.data(), need * sizeof(int32_t));
+  for (size_t i = 0; i < plan->work.size(); ++i)
+    std::memcpy(out + i * pkv::kWorkItemPublicFields, &plan->work[i], pkv::kWorkItemPublicFields * sizeof(int32_t));
   return PKV_OK;
 }
 

@@ -73,13 +73,52 @@ __device__ __forceinline__ int o_dim(int mb, int j, int g) {
   }
 }
 
+// acc[k] += sum over the ns partials of weight(partial, row of column k) * partial[column k], for
+// the NC float4 columns col[k] < n4 of this thread, U partial reads per column in flight.
+template <int NC, int U, int HEADS, int NA>
+__device__ __forceinline__ void merge_accumulate(float4 (&acc)[NA], const int (&col)[NA], const int (&crow)[NA], int n4,
+                                                 const float4* base, int ns, const float* wgt, int slot4) {
+  int sp = 0;
+  for (; sp + U <= ns; sp += U) {
+    float4 x[U][NC];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < NC; ++k)
+        x[u][k] = col[k] < n4 ? __ldcg(base + (int64_t)(sp + u) * slot4 + col[k]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        const float wv = wgt[(sp + u) * HEADS + (col[k] < n4 ? crow[k] : 0)];
+        acc[k].x += wv * x[u][k].x;
+        acc[k].y += wv * x[u][k].y;
+        acc[k].z += wv * x[u][k].z;
+        acc[k].w += wv * x[u][k].w;
+      }
+  }
+  for (; sp < ns; ++sp) {
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      if (col[k] < n4) {
+        const float4 x = __ldcg(base + (int64_t)sp * slot4 + col[k]);
+        const float wv = wgt[sp * HEADS + crow[k]];
+        acc[k].x += wv * x.x;
+        acc[k].y += wv * x.y;
+        acc[k].z += wv * x.z;
+        acc[k].w += wv * x.w;
+      }
+    }
+  }
+}
+
 template <int D, bool FP8, int NB>
 __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kernel(const RunParams p, int32_t* err) {
   using C = DecodeCfg<D, FP8, NB>;
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_stage_key[C::WARPS][C::STAGES];
 
   const WorkItem w = p.work[blockIdx.x];
-  const ReqInfo ri = p.req[w.req];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
@@ -111,9 +150,6 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   // ---- per-warp cp.async ring ----
   uint8_t* wsm = smem + warp * C::WARP_SMEM;
   const uint32_t wsm_u = smem_u32(wsm);
-  const int n_keys = w.kv_end - w.kv_begin;
-  const int n_tiles = (n_keys + C::KEYS - 1) / C::KEYS;
-  const int my_tiles = n_tiles > warp ? (n_tiles - warp + C::WARPS - 1) / C::WARPS : 0;
   const int lr = lane & 15;  // row whose page this lane resolves
   const int64_t head_off = (int64_t)w.kv_head * p.stride_head_b;
 
@@ -126,17 +162,46 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   const int ps_shift = (ps & (ps - 1)) == 0 ? __ffs(ps) - 1 : -1;  // page sizes are usually powers of 2
   auto page_of = [&](int key) -> int { return ps_shift >= 0 ? key >> ps_shift : key / ps; };
   const int64_t row_step = (int64_t)RPI * p.stride_token_b;  // bytes between the rows of consecutive instructions
-  // The page id of the row this lane resolves is fetched one tile ahead (this warp's next tile is
-  // 4 tiles = 64 keys further), so the index load never stalls the issue of the copies.
-  auto fetch_page = [&](int key) -> int {
-    return key < w.kv_end ? __ldg(p.kv_indices + ri.page_base + page_of(key)) : 0;
+
+  // ---- the warp's tile sequence ----
+  // Alone on its range (num_splits == 1) a warp takes every 4th 16-key tile.  When num_splits CTAs
+  // share the range, it is cut into 32-key groups: warp w of split s starts on group 4 s + w and
+  // then claims group 4 num_splits + atomicAdd(claim, 1), and so on, until the groups run out (so
+  // the warps of all the CTAs end within about one group of each other).  The claim for the next
+  // group is sent when the warp starts loading a group, 2 tiles before it is needed.  A key >=
+  // kv_end ends the sequence.
+  constexpr int GROUP_KEYS = 2 * C::KEYS;
+  const bool shared_range = w.num_splits > 1;
+  const int claim_base = w.num_splits * C::WARPS;
+  int pending = 0;  // lane 0: value returned by the outstanding claim
+  if (shared_range && lane == 0) pending = atomicAdd(p.claim + w.unit * kClaimStride, 1);
+  auto next_key = [&](int k) -> int {  // first key of the tile after the one starting at k (k < kv_end)
+    if (!shared_range) return k + C::WARPS * C::KEYS;
+    if (((k - w.kv_begin) & (GROUP_KEYS - 1)) != GROUP_KEYS - C::KEYS) return k + C::KEYS;
+    const int grp = claim_base + __shfl_sync(0xffffffffu, pending, 0);
+    const int nk = grp < (w.kv_end - w.kv_begin + GROUP_KEYS - 1) / GROUP_KEYS ? w.kv_begin + grp * GROUP_KEYS : w.kv_end;
+    if (nk < w.kv_end && lane == 0) pending = atomicAdd(p.claim + w.unit * kClaimStride, 1);
+    return nk;
   };
-  int next_page = fetch_page(w.kv_begin + warp * C::KEYS + lr);
-  auto load_tile = [&](int i, int stage) {
-    const int key0 = w.kv_begin + (warp + i * C::WARPS) * C::KEYS;
+  int lkey = w.kv_begin + (shared_range ? (w.split * C::WARPS + warp) * GROUP_KEYS : warp * C::KEYS);
+  lkey = min(lkey, w.kv_end);
+  int nkey = lkey < w.kv_end ? next_key(lkey) : w.kv_end;
+  int* key_of_stage = s_stage_key[warp];  // first key of the tile in each ring stage (kv_end: none)
+
+  // The page id of the row this lane resolves is fetched one tile ahead, so the index load never
+  // stalls the issue of the copies.
+  auto fetch_page = [&](int key) -> int {
+    return key < w.kv_end ? __ldg(p.kv_indices + w.page_base + page_of(key)) : 0;
+  };
+  int next_page = fetch_page(lkey + lr);
+  // Load the tile starting at lkey into `stage` and advance the sequence.
+  auto load_tile = [&](int stage) {
+    const int key0 = lkey;
     const int key = key0 + lr;
     const int page = next_page;
-    next_page = fetch_page(key + C::WARPS * C::KEYS);
+    next_page = fetch_page(nkey + lr);
+    lkey = nkey;
+    nkey = nkey < w.kv_end ? next_key(nkey) : w.kv_end;
     const uint32_t dk = wsm_u + stage * 2 * C::TILE_B;
     const uint32_t dv = dk + C::TILE_B;
     // Common case: all 16 keys present and on one page (page size >= 16, chunk starts aligned), so
@@ -188,7 +253,8 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
 
 #pragma unroll
   for (int s = 0; s < C::STAGES - 1; ++s) {
-    if (s < my_tiles) load_tile(s, s);
+    if (lane == 0) key_of_stage[s] = lkey;
+    if (lkey < w.kv_end) load_tile(s);
     cp_async_commit();
   }
 
@@ -197,22 +263,21 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   const int k_key = ((mi & 1) << 3) + rr;  // matrices: (keys 0-7, c), (keys 8-15, c), (keys 0-7, c+1), (8-15, c+1)
   const int v_key = ((mi >> 1) << 3) + rr; // matrices: (keys 0-7, c), (keys 0-7, c+1), (keys 8-15, c), (8-15, c+1)
 
-  int stage = 0, fill = C::STAGES - 1;  // ring slot of tile i and of tile i + STAGES - 1
-  for (int i = 0; i < my_tiles; ++i) {
+  int stage = 0, fill = C::STAGES - 1;  // ring slot of the tile computed now and of the one loaded now
+  while (true) {
     cp_async_wait<C::STAGES - 2>();
     __syncwarp();
-    // refill the stage tile i-1 used (consumed in the previous iteration) before computing tile i,
-    // so STAGES-1 tiles stay in flight during the compute
-    {
-      const int nx = i + C::STAGES - 1;
-      if (nx < my_tiles) load_tile(nx, fill);
-      cp_async_commit();
-      fill = fill + 1 == C::STAGES ? 0 : fill + 1;
-    }
+    const int key0 = key_of_stage[stage];
+    if (key0 >= w.kv_end) break;
+    // refill the stage the previous tile used before computing this one, so STAGES-1 tiles stay
+    // in flight during the compute
+    if (lane == 0) key_of_stage[fill] = lkey;
+    if (lkey < w.kv_end) load_tile(fill);
+    cp_async_commit();
+    fill = fill + 1 == C::STAGES ? 0 : fill + 1;
     const uint32_t kb = wsm_u + stage * 2 * C::TILE_B;
     const uint32_t vb = kb + C::TILE_B;
     stage = stage + 1 == C::STAGES ? 0 : stage + 1;
-    const int key0 = w.kv_begin + (warp + i * C::WARPS) * C::KEYS;
 
     // ---- S^T = K Q^T for 16 keys ----
     float s[NB][4];
@@ -419,7 +484,7 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
-    const int unit = p.slot_unit[w.out_slot];
+    const int unit = w.unit;
     const MergeItem mi_ = p.merge[unit];
     if (threadIdx.x == 0) {
       const int done = atomicAdd(p.unit_count + unit, 1);
@@ -430,7 +495,7 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     __threadfence();
     // Online merge over chunks of splits: the chunk's log2-sum-exps are staged in shared memory by
     // all threads and turned into per-row weights 2^(lse_s - M) once; each thread owns float4 columns
-    // of the output and reads 8 partials per round, so 8 L2 reads per column are in flight.
+    // of the output and keeps 8-16 partial reads per column in flight.
     constexpr int V4 = C::HEADS * D / 4;            // float4s of the (at most HEADS) output rows
     constexpr int PER_T = (V4 + 127) / 128;         // float4s per thread
     constexpr int SLOT4 = kDecodeRows * D / 4;      // float4s between consecutive partials
@@ -488,38 +553,10 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
         }
       }
       const float4* base = pm + (int64_t)s0 * SLOT4;
-      int sp = 0;
-      for (; sp + 8 <= ns; sp += 8) {
-        float4 x[8][PER_T];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-          for (int k = 0; k < PER_T; ++k)
-            x[u][k] = col[k] < n4 ? __ldcg(base + (int64_t)(sp + u) * SLOT4 + col[k]) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-          for (int k = 0; k < PER_T; ++k) {
-            const float wv = wgt[(sp + u) * C::HEADS + (col[k] < n4 ? crow[k] : 0)];
-            acc[k].x += wv * x[u][k].x;
-            acc[k].y += wv * x[u][k].y;
-            acc[k].z += wv * x[u][k].z;
-            acc[k].w += wv * x[u][k].w;
-          }
-      }
-      for (; sp < ns; ++sp) {
-#pragma unroll
-        for (int k = 0; k < PER_T; ++k) {
-          if (col[k] < n4) {
-            const float4 x = __ldcg(base + (int64_t)sp * SLOT4 + col[k]);
-            const float wv = wgt[sp * C::HEADS + crow[k]];
-            acc[k].x += wv * x.x;
-            acc[k].y += wv * x.y;
-            acc[k].z += wv * x.z;
-            acc[k].w += wv * x.w;
-          }
-        }
-      }
+      if (n4 <= 128)  // one column per thread (up to 4 rows of 128 dims): 16 reads in flight
+        merge_accumulate<1, 16, C::HEADS>(acc, col, crow, n4, base, ns, wgt, SLOT4);
+      else
+        merge_accumulate<PER_T, 8, C::HEADS>(acc, col, crow, n4, base, ns, wgt, SLOT4);
     }
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((int64_t)mi_.q_row * p.num_qo_heads + qh0) * D;
 #pragma unroll
@@ -535,7 +572,10 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     if (p.lse && threadIdx.x < rows)
       p.lse[(int64_t)mi_.q_row * p.num_qo_heads + qh0 + threadIdx.x] =
           (sM[threadIdx.x] + __log2f(sW[threadIdx.x])) * 0.69314718055994531f;
-    if (threadIdx.x == 0) p.unit_count[unit] = 0;  // ready for the next run of this plan
+    if (threadIdx.x == 0) {  // ready for the next run of this plan
+      p.unit_count[unit] = 0;
+      atomicExch(p.claim + unit * kClaimStride, 0);
+    }
   }
 }
 

@@ -92,12 +92,11 @@ extern "C" int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, 
   char* base = static_cast<char*>(ws);
   // the plan's metadata, straight from its host arrays (stream-ordered before the kernels)
   struct Seg { size_t off; const void* src; size_t bytes; };
-  const Seg segs[5] = {
+  const Seg segs[4] = {
       {plan->off_work, plan->work.data(), plan->work.size() * sizeof(WorkItem)},
       {plan->off_merge, plan->merge.data(), plan->merge.size() * sizeof(MergeItem)},
       {plan->off_req, plan->req.data(), plan->req.size() * sizeof(ReqInfo)},
       {plan->off_idx, plan->indices.data(), plan->indices.size() * sizeof(int32_t)},
-      {plan->off_slot_unit, plan->slot_unit.data(), plan->slot_unit.size() * sizeof(int32_t)},
   };
   for (const Seg& g : segs) {
     if (!g.bytes) continue;
@@ -105,7 +104,7 @@ extern "C" int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, 
     if (e != cudaSuccess) return noalloc_fail(PKV_ECUDA, std::string("metadata copy: ") + cudaGetErrorString(e));
   }
   if (!plan->merge.empty()) {
-    e = cudaMemsetAsync(base + plan->off_count, 0, plan->merge.size() * sizeof(int32_t), s);
+    e = cudaMemsetAsync(base + plan->off_count, 0, plan->off_plse - plan->off_count, s);
     if (e != cudaSuccess) return noalloc_fail(PKV_ECUDA, std::string("counter reset: ") + cudaGetErrorString(e));
   }
 
@@ -116,8 +115,8 @@ extern "C" int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, 
   p.kv_indices = reinterpret_cast<const int32_t*>(base + plan->off_idx);
   p.part_lse = reinterpret_cast<float*>(base + plan->off_plse);
   p.part_o = reinterpret_cast<float*>(base + plan->off_po);
-  p.slot_unit = reinterpret_cast<const int32_t*>(base + plan->off_slot_unit);
   p.unit_count = reinterpret_cast<int32_t*>(base + plan->off_count);
+  p.claim = reinterpret_cast<int32_t*>(base + plan->off_claim);
   p.q = q;
   p.o = o;
   p.lse = lse;

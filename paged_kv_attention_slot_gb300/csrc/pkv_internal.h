@@ -10,18 +10,23 @@
 
 namespace pkv {
 
-// One CTA of a run kernel.  Same field order as the public pkv_plan_work_items() rows.
+// One CTA of a run kernel.  The first 8 fields are the public pkv_plan_work_items() rows.
 struct WorkItem {
   int32_t req;         // request index
   int32_t kv_head;     // KV head
   int32_t head_group;  // group of up to 16 query heads of this KV head (decode); 0 (prefill)
-  int32_t kv_begin;    // first key (logical position) this CTA reads
-  int32_t kv_end;      // one past the last key this CTA reads
+  int32_t kv_begin;    // first key (logical position) of the range this CTA draws from
+  int32_t kv_end;      // one past the last key of that range
   int32_t q_row;       // first token row of Q / O
   int32_t out_slot;    // decode: partial slot, or -1 = write the final output
   int32_t q_rows;      // tokens of this request in this CTA's tile (decode: 1)
+  int32_t page_base;   // first kv_indices entry of the request
+  int32_t split;       // decode: index of this CTA among the CTAs sharing [kv_begin, kv_end)
+  int32_t num_splits;  // decode: CTAs sharing the range (1 = this CTA reads all of it)
+  int32_t unit;        // decode: merge item of the shared range, or -1
 };
-static_assert(sizeof(WorkItem) == 32, "WorkItem is 32 bytes");
+static_assert(sizeof(WorkItem) == 48, "WorkItem is 48 bytes");
+constexpr int kWorkItemPublicFields = 8;
 
 // One (request, KV head, head group) whose split-KV partials must be merged.
 struct MergeItem {
@@ -43,6 +48,10 @@ struct ReqInfo {
 };
 static_assert(sizeof(ReqInfo) == 16, "ReqInfo is 16 bytes");
 
+// Each split unit's claim counter sits on its own 128-byte line: every warp of the unit's CTAs
+// updates it once per key group, and counters sharing a line would serialise in one L2 slice.
+constexpr int kClaimStride = 32;
+
 // Max query rows one decode CTA handles per KV head (one m16 MMA tile).
 constexpr int kDecodeRows = 16;
 
@@ -54,8 +63,8 @@ struct RunParams {
   const int32_t* kv_indices;
   float* part_o;    // [num_partials, 16, head_dim]
   float* part_lse;  // [num_partials, 16] (log2 units)
-  const int32_t* slot_unit;  // [num_partials]: merge item of each partial slot
   int32_t* unit_count;       // [num_merge]: partials written so far (0 between runs)
+  int32_t* claim;            // [num_merge * kClaimStride]: groups claimed beyond the static ones (0 between runs)
   const void* q;
   void* o;
   float* lse;  // nullable
@@ -103,9 +112,7 @@ struct pkv_plan {
   std::vector<pkv::MergeItem> merge;
   std::vector<pkv::ReqInfo> req;
   std::vector<int32_t> indices;
-  size_t off_work = 0, off_merge = 0, off_req = 0, off_idx = 0, off_slot_unit = 0, off_count = 0, off_plse = 0,
-         off_po = 0;
-  std::vector<int32_t> slot_unit;
+  size_t off_work = 0, off_merge = 0, off_req = 0, off_idx = 0, off_count = 0, off_claim = 0, off_plse = 0, off_po = 0;
   size_t meta_bytes = 0, need_bytes = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
