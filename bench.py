@@ -54,6 +54,10 @@ def _src_hash(*names):
     return h.hexdigest()[:16]
 
 
+DECODE_SOURCES = ["decode.cu", "ptx.cuh", "pkv_internal.h"]
+PREFILL_SOURCES = ["prefill.cu", "ptx.cuh", "tc.cuh", "pkv_internal.h"]
+
+
 def _traffic(kernel: str, source_files):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -418,9 +422,10 @@ def decode_other_configs(device, hbm):
     import workloads as W
 
     res = []
-    for n, window, name in ((4, -1, "llama70b_ragged_decode: batch 256, 64 q / 8 kv, log-normal KV (median 1024), page 64, bf16"),
-                            (5, -1, "fp8_long_decode: batch 2, KV 131072, 32 q / 8 kv, page 128, FP8 E4M3 KV"),
-                            (5, 4096, "fp8_long_decode_window: as above, sliding window 4096")):
+    for n, window, key, name in (
+            (4, -1, "decode_llama70b_ragged", "llama70b_ragged_decode: batch 256, 64 q / 8 kv, log-normal KV (median 1024), page 64, bf16"),
+            (5, -1, "decode_fp8_long", "fp8_long_decode: batch 2, KV 131072, 32 q / 8 kv, page 128, FP8 E4M3 KV"),
+            (5, 4096, "decode_fp8_long_window", "fp8_long_decode_window: as above, sliding window 4096")):
         b = W.workload(n, window_left=window)
         st = _device_state(b, device)
         plan = pk.Plan()
@@ -430,6 +435,7 @@ def decode_other_configs(device, hbm):
         gbs = b.kv_bytes_read() / (k_ms * 1e-3) / 1e9
         res.append({"workload": name, "kv_bytes": b.kv_bytes_read(), "kernel_ms": round(k_ms, 4),
                     "achieved": round(gbs, 2), "unit": "GB/s", "frac": round(gbs / hbm, 4), "timing": mode,
+                    "traffic": _traffic(key, DECODE_SOURCES),
                     "plan": {"ctas": info["num_work"], "merge_units": info["num_merge"], "kv_chunk": info["kv_chunk"]}})
         del st, plan
         torch.cuda.empty_cache()
@@ -469,7 +475,7 @@ def prefill_measure(device, steps, warmup, peak_tflops):
         "flops_per_step": flops,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_tflops, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tflops, 4), "kernel_ms": round(k_ms, 4), "timing": k_mode,
-                     "traffic": _traffic("prefill", ["prefill.cu", "ptx.cuh", "tc.cuh"])},
+                     "traffic": _traffic("prefill", PREFILL_SOURCES)},
         "run_ms_mean_in_steps": round(run_avg, 4),
         "gpu_launches_per_step": 2,
     }
@@ -587,7 +593,7 @@ def main():
                          "kernel": "decode_kernel (split-KV merge fused), one launch per decode_run",
                          "kernel_ms": round(k_ms, 4), "timing": k_mode,
                          "run_ms_mean_in_steps": round(run_avg, 4),
-                         "traffic": _traffic("decode", ["decode.cu", "ptx.cuh"])},
+                         "traffic": _traffic("decode", DECODE_SOURCES)},
             "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
