@@ -9,11 +9,13 @@
 //
 // GB300 design.  Decode is HBM-bound (about G flops per byte of KV), so the kernel is built around
 // streaming the pages at full bandwidth while keeping the per-key work short:
-//  * one CTA = 4 warps = one work item (request, KV head, group of <= 16 query heads, KV chunk); the
-//    planner cuts long sequences into equal chunks and launches CTAs longest first;
+//  * one CTA = 4 warps = one work item (request, KV head, group of <= 16 query heads) with a key
+//    range; a range short enough for one CTA is read by it alone (each warp takes every 4th 16-key
+//    tile), a long one is shared by several CTAs whose warps claim 32-key groups of it from a
+//    per-range counter at run time, so the CTAs of a range finish together;
 //  * every warp runs its own cp.async ring (16 keys per stage, K and V rows gathered page by page
-//    through kv_indices, 16-byte vectors, XOR-swizzled so ldmatrix reads are conflict-free) and takes
-//    every 4th 16-key tile of the chunk, so no CTA-wide barrier sits in the main loop;
+//    through kv_indices, 16-byte vectors, XOR-swizzled so ldmatrix reads are conflict-free), so no
+//    CTA-wide barrier sits in the main loop;
 //  * the products run on m16n8k16 tensor-core MMAs with the KEYS in M and the (<= 8 per n-block)
 //    query heads of one KV head in N: S^T = K Q^T, then O^T += V^T P^T.  Each K/V row is read once
 //    per KV head, a 16-key tile costs 8 MMAs per product (not 16 with heads in M), and the output
