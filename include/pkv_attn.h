@@ -56,7 +56,13 @@ typedef enum {
 
 typedef enum {
   PKV_MODE_DECODE = 0,  /* one new token per request (qo_indptr[i+1] - qo_indptr[i] in {0, 1}) */
-  PKV_MODE_PREFILL = 1  /* any number of new tokens per request (prefill / prefix-cached extend) */
+  PKV_MODE_PREFILL = 1, /* any number of new tokens per request (prefill / prefix-cached extend) */
+  PKV_MODE_MIXED = 2    /* both in one batch: requests with one new token are planned for the
+                         * decode kernel, requests with more for the prefill kernel, and the two
+                         * runs write their rows of one output (the decode / prefill-extend split
+                         * of "vLLM Attention 后端与 FlashInfer 元数据", sections «为什么先把 Decode 移到前面»
+                         * and «FlashInfer Builder 的结果»).  Requests may come in any order: every
+                         * CTA carries its own token row, so no decode-first reordering is needed. */
 } pkv_mode;
 
 /* Device error codes a kernel may record (read with pkv_device_error). */
@@ -208,9 +214,12 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
  *        scores of each row (the statistic "SGLang 源码完全拆解(八)：Attention Backend", section
  *        «extend 的两种形态», merges states with).
  * The cache geometry (heads, head_dim, dtype) must match the plan, and the plan's largest page id
- * must be < cache->num_pages (checked on the host, O(1)).  decode_run needs a PKV_MODE_DECODE plan,
- * prefill_run a PKV_MODE_PREFILL plan.  Rows of requests with n_i == 0 do not exist; no other row
- * of o is left unwritten.  The runs allocate nothing, read no host data of the batch and never
+ * must be < cache->num_pages (checked on the host, O(1)).  decode_run needs a PKV_MODE_DECODE or
+ * PKV_MODE_MIXED plan, prefill_run a PKV_MODE_PREFILL or PKV_MODE_MIXED plan; on a mixed plan each
+ * writes only its own rows (decode_run the rows of one-token requests, prefill_run the others), and
+ * both must run for o to be complete (in either order; they touch disjoint rows).  A run with no
+ * rows of its kind launches nothing.  Rows of requests with n_i == 0 do not exist; no other row of
+ * o is left unwritten.  The runs allocate nothing, read no host data of the batch and never
  * synchronise; several runs (e.g. one per layer) may share one plan as long as the workspace is not
  * used by two runs at the same time.
  */
@@ -267,6 +276,11 @@ typedef struct pkv_plan_info {
   int64_t workspace_bytes;
   int64_t max_page_id;    /* -1 if the batch has no pages                                  */
   int64_t kv_tokens;      /* sum over requests of the keys the plan reads (per KV head)     */
+  int64_t num_decode_work;    /* CTAs of the decode kernel (the first num_decode_work items)  */
+  int64_t num_decodes;        /* requests planned for the decode kernel                      */
+  int64_t num_decode_tokens;  /* their token rows                                            */
+  int64_t num_prefills;       /* requests planned for the prefill kernel                     */
+  int64_t num_prefill_tokens; /* their token rows                                            */
 } pkv_plan_info;
 
 int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info);

@@ -142,7 +142,8 @@ class Plan:
               mode, window_left, sm_scale, kv_dtype, max_splits, num_sms):
         arrs = [_i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)]
         B = len(arrs[3])
-        m = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL}[mode]
+        m = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL,
+             "mixed": _lib.PKV_MODE_MIXED}[mode]
         kd = {"bf16": _lib.PKV_BF16, "e4m3": _lib.PKV_FP8_E4M3, "fp8": _lib.PKV_FP8_E4M3}[kv_dtype]
         a = _lib.pkv_plan_args(B, _ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(arrs[3]), num_qo_heads,
                                num_kv_heads, head_dim, page_size, m, 1, window_left, float(sm_scale),
@@ -211,9 +212,15 @@ class Plan:
             out = torch.empty_like(q)
         if (return_lse or lse is not None) and lse is None:
             lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
-        fn = lib().pkv_attn_decode_run if self.mode == "decode" else lib().pkv_attn_prefill_run
-        check(fn(self._h, q.data_ptr(), C.byref(cache.struct), out.data_ptr(),
-                 lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
+        if self.mode == "decode":
+            fns = [lib().pkv_attn_decode_run]
+        elif self.mode == "mixed":  # one-token rows on the decode kernel, the rest on the prefill kernel
+            fns = [lib().pkv_attn_decode_run, lib().pkv_attn_prefill_run]
+        else:
+            fns = [lib().pkv_attn_prefill_run]
+        for fn in fns:
+            check(fn(self._h, q.data_ptr(), C.byref(cache.struct), out.data_ptr(),
+                     lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
         return (out, lse) if (return_lse or lse is not None) else out
 
 

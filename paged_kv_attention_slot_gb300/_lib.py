@@ -24,6 +24,7 @@ PKV_BF16 = 0
 PKV_FP8_E4M3 = 1
 PKV_MODE_DECODE = 0
 PKV_MODE_PREFILL = 1
+PKV_MODE_MIXED = 2
 
 STATUS_NAMES = {0: "PKV_OK", -1: "PKV_EINVAL", -2: "PKV_EUNSUPPORTED", -3: "PKV_EWORKSPACE", -4: "PKV_ECUDA",
                 -5: "PKV_EDEVICE"}
@@ -90,6 +91,11 @@ class pkv_plan_info(C.Structure):
         ("workspace_bytes", C.c_int64),
         ("max_page_id", C.c_int64),
         ("kv_tokens", C.c_int64),
+        ("num_decode_work", C.c_int64),
+        ("num_decodes", C.c_int64),
+        ("num_decode_tokens", C.c_int64),
+        ("num_prefills", C.c_int64),
+        ("num_prefill_tokens", C.c_int64),
     ]
 
 

@@ -82,11 +82,12 @@ inline int32_t item_share(const WorkItem& x) {
 
 // Order the work list longest first (stable counting sort on the per-CTA share, bucketed so that
 // at most 4096 buckets are used: the order is exact up to 1/4096 of the longest share).
-void order_longest_first(std::vector<WorkItem>& w) {
-  const size_t n = w.size();
+void order_longest_first(std::vector<WorkItem>& all, size_t begin, size_t end) {
+  const size_t n = end - begin;
   if (n < 2) return;
+  WorkItem* w = all.data() + begin;
   int32_t maxlen = 0;
-  for (const WorkItem& x : w) maxlen = std::max(maxlen, item_share(x));
+  for (size_t i = 0; i < n; ++i) maxlen = std::max(maxlen, item_share(w[i]));
   int shift = 0;
   while ((maxlen >> shift) >= 4096) ++shift;
   const int nb = (maxlen >> shift) + 1;
@@ -95,12 +96,12 @@ void order_longest_first(std::vector<WorkItem>& w) {
   count.assign(nb + 1, 0u);
   tmp.resize(n);
   uint32_t* c = count.data();
-  const WorkItem* src = w.data();
+  const WorkItem* src = w;
   for (size_t i = 0; i < n; ++i) ++c[nb - (item_share(src[i]) >> shift)];
   for (int d = 0; d < nb; ++d) c[d + 1] += c[d];
   WorkItem* dst = tmp.data();
   for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - (item_share(src[i]) >> shift)]++] = src[i];
-  w.swap(tmp);
+  std::memcpy(w, dst, n * sizeof(WorkItem));
 }
 
 // Validate the arguments and build the work list into P (no device work).
@@ -115,7 +116,8 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     return fail(PKV_EINVAL, "num_qo_heads must be a multiple of num_kv_heads");
   if (a->head_dim != 64 && a->head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
   if (a->page_size < 1) return fail(PKV_EINVAL, "page_size must be >= 1");
-  if (a->mode != PKV_MODE_DECODE && a->mode != PKV_MODE_PREFILL) return fail(PKV_EINVAL, "unknown mode");
+  if (a->mode != PKV_MODE_DECODE && a->mode != PKV_MODE_PREFILL && a->mode != PKV_MODE_MIXED)
+    return fail(PKV_EINVAL, "unknown mode");
   if (a->causal != 1) return fail(PKV_EUNSUPPORTED, "only causal (bottom-right aligned) attention is implemented");
   if (a->window_left < -1) return fail(PKV_EINVAL, "window_left must be -1 or >= 0");
   if (!(std::isfinite(a->sm_scale))) return fail(PKV_EINVAL, "sm_scale is not finite");
@@ -125,11 +127,15 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     return fail(PKV_EUNSUPPORTED, "FP8 KV needs head_dim 128");
   if (a->max_splits < 0) return fail(PKV_EINVAL, "max_splits < 0");
   const int32_t G = a->num_qo_heads / a->num_kv_heads;
-  if (a->mode == PKV_MODE_PREFILL) {
+  // requests with more than one new token go to the prefill kernel (all of them in prefill mode)
+  bool any_extend = a->mode == PKV_MODE_PREFILL;
+  if (a->mode == PKV_MODE_MIXED)
+    for (int32_t i = 0; i < B && !any_extend; ++i) any_extend = a->qo_indptr[i + 1] - a->qo_indptr[i] > 1;
+  if (any_extend) {
     const char* why = nullptr;
     if (!pkv::prefill_supported(&why)) return fail(PKV_EUNSUPPORTED, why ? why : "prefill kernel unavailable");
-    if (a->head_dim != 128) return fail(PKV_EUNSUPPORTED, "prefill needs head_dim 128");
-    if (a->kv_dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "prefill needs a bf16 KV cache");
+    if (a->head_dim != 128) return fail(PKV_EUNSUPPORTED, "prefill / extend rows need head_dim 128");
+    if (a->kv_dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "prefill / extend rows need a bf16 KV cache");
     if (G > kPrefillRows || kPrefillRows % G) return fail(PKV_EUNSUPPORTED, "prefill needs 128 % (Hq/Hkv) == 0");
   }
 
@@ -196,15 +202,22 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   P->num_partials = 0;
   P->kv_tokens = 0;
   P->kv_chunk = 0;
+  P->num_decode_work = 0;
+  P->num_decodes = P->num_decode_tokens = P->num_prefills = P->num_prefill_tokens = 0;
 
-  if (a->mode == PKV_MODE_DECODE) {
+  // decode rows: every request in decode mode, the one-token requests in mixed mode
+  const bool plan_decode = a->mode == PKV_MODE_DECODE || a->mode == PKV_MODE_MIXED;
+  const bool plan_prefill = a->mode == PKV_MODE_PREFILL || a->mode == PKV_MODE_MIXED;
+  if (plan_decode) {
     const int32_t groups = (G + pkv::kDecodeRows - 1) / pkv::kDecodeRows;
     struct Unit { int32_t req, lo, hi; };
     std::vector<Unit> units;
     units.reserve(B);
     int64_t total = 0;
     for (int32_t i = 0; i < B; ++i) {
-      if (P->req[i].q_len == 0) continue;
+      if (P->req[i].q_len != 1) continue;
+      ++P->num_decodes;
+      ++P->num_decode_tokens;
       const int32_t L = P->req[i].kv_len;
       const int32_t pos = L - 1;
       const int32_t lo = a->window_left >= 0 ? std::max(0, pos - a->window_left) : 0;
@@ -299,10 +312,15 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
       }
     }
     P->num_partials = slot;
-  } else {
+  }
+  P->num_decode_work = (int64_t)P->work.size();
+  if (plan_prefill) {
     const int32_t tok_per_tile = kPrefillTiles * (kPrefillRows / G);  // tokens per CTA
     for (int32_t i = 0; i < B; ++i) {
       const ReqInfo& r = P->req[i];
+      if (r.q_len == 0 || (a->mode == PKV_MODE_MIXED && r.q_len == 1)) continue;
+      ++P->num_prefills;
+      P->num_prefill_tokens += r.q_len;
       for (int32_t t0 = 0; t0 < r.q_len; t0 += tok_per_tile) {
         const int32_t rows = std::min(tok_per_tile, r.q_len - t0);
         const int32_t pos0 = r.kv_len - r.q_len + t0;
@@ -329,7 +347,8 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     }
   }
   // longest first: the block scheduler hands out CTAs roughly in launch order
-  order_longest_first(P->work);
+  order_longest_first(P->work, 0, (size_t)P->num_decode_work);
+  order_longest_first(P->work, (size_t)P->num_decode_work, P->work.size());
   if ((int64_t)P->work.size() > INT32_MAX) return fail(PKV_EUNSUPPORTED, "too many CTAs");
 
   // workspace layout: [work][merge][req][kv_indices] | [partial lse][partial o]
@@ -378,10 +397,12 @@ int check_cache(const pkv_plan* P, const pkv_cache* c) {
   return PKV_OK;
 }
 
-pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c, void* o, float* lse) {
+// Kernel parameters for the work items [first, first + count) of the plan.
+pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c, void* o, float* lse, int64_t first,
+                           int64_t count) {
   pkv::RunParams p{};
   char* ws = (char*)P->ws;
-  p.work = (const WorkItem*)(ws + P->off_work);
+  p.work = (const WorkItem*)(ws + P->off_work) + first;
   p.merge = (const MergeItem*)(ws + P->off_merge);
   p.req = (const ReqInfo*)(ws + P->off_req);
   p.kv_indices = (const int32_t*)(ws + P->off_idx);
@@ -408,7 +429,7 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
   const float log2e = 1.4426950408889634f;
   p.scale_log2 = P->sm_scale * log2e * (c->dtype == PKV_FP8_E4M3 ? c->k_scale : 1.0f);
   p.out_scale = c->dtype == PKV_FP8_E4M3 ? c->v_scale : 1.0f;
-  p.num_work = (int64_t)P->work.size();
+  p.num_work = count;
   p.num_merge = (int64_t)P->merge.size();
   return p;
 }
@@ -416,9 +437,9 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
 int check_run(const pkv_plan* P, int mode, const void* q, const pkv_cache* c, void* o) {
   if (!P || !P->valid) return fail(PKV_EINVAL, "plan is NULL or has not been planned");
   if (!P->ws) return fail(PKV_EINVAL, "the plan is host-only (planned without a workspace)");
-  if (P->mode != mode)
-    return fail(PKV_EINVAL, mode == PKV_MODE_DECODE ? "decode_run needs a PKV_MODE_DECODE plan"
-                                                    : "prefill_run needs a PKV_MODE_PREFILL plan");
+  if (P->mode != mode && P->mode != PKV_MODE_MIXED)
+    return fail(PKV_EINVAL, mode == PKV_MODE_DECODE ? "decode_run needs a PKV_MODE_DECODE or PKV_MODE_MIXED plan"
+                                                    : "prefill_run needs a PKV_MODE_PREFILL or PKV_MODE_MIXED plan");
   int st = check_cache(P, c);
   if (st != PKV_OK) return st;
   if (P->total_tokens > 0 && (!q || !o)) return fail(PKV_EINVAL, "q and o must be non-NULL");
@@ -572,8 +593,8 @@ int pkv_attn_decode_run(const pkv_plan* plan, const void* q, const pkv_cache* ca
                         void* stream) {
   int st = check_run(plan, PKV_MODE_DECODE, q, cache, o);
   if (st != PKV_OK) return st;
-  if (plan->work.empty()) return PKV_OK;
-  pkv::RunParams p = make_params(plan, q, cache, o, lse);
+  if (plan->num_decode_work == 0) return PKV_OK;
+  pkv::RunParams p = make_params(plan, q, cache, o, lse, 0, plan->num_decode_work);
   PKV_CUDA(pkv::launch_decode(p, cache->dtype, (cudaStream_t)stream), "decode launch");
   return PKV_OK;
 }
@@ -582,7 +603,8 @@ int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* c
                          void* stream) {
   int st = check_run(plan, PKV_MODE_PREFILL, q, cache, o);
   if (st != PKV_OK) return st;
-  if (plan->work.empty()) return PKV_OK;
+  const int64_t first = plan->num_decode_work, count = (int64_t)plan->work.size() - first;
+  if (count == 0) return PKV_OK;
   if (cache->stride_page != (int64_t)cache->page_size * cache->stride_token)
     return fail(PKV_EUNSUPPORTED, "prefill needs stride_page == page_size * stride_token (uniform slot rows)");
   if (cache->stride_head != cache->head_dim)
@@ -619,7 +641,7 @@ int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* c
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(V) failed: " + std::to_string((int)r));
   }
-  pkv::RunParams p = make_params(plan, q, cache, o, lse);
+  pkv::RunParams p = make_params(plan, q, cache, o, lse, first, count);
   PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
   return PKV_OK;
 }
@@ -644,6 +666,11 @@ int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info) {
   info->workspace_bytes = (int64_t)plan->need_bytes;
   info->max_page_id = plan->max_page_id;
   info->kv_tokens = plan->kv_tokens;
+  info->num_decode_work = plan->num_decode_work;
+  info->num_decodes = plan->num_decodes;
+  info->num_decode_tokens = plan->num_decode_tokens;
+  info->num_prefills = plan->num_prefills;
+  info->num_prefill_tokens = plan->num_prefill_tokens;
   return PKV_OK;
 }
 

@@ -108,6 +108,8 @@ struct pkv_plan {
   int32_t mode = 0, batch = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, window_left = -1, kv_dtype = 0, q_dtype = 0;
   float sm_scale = 0.f;
   int64_t total_tokens = 0, max_page_id = -1, kv_tokens = 0, kv_chunk = 0, num_partials = 0;
+  int64_t num_decode_work = 0;  // the decode kernel's items come first in `work`, the prefill kernel's after
+  int64_t num_decodes = 0, num_decode_tokens = 0, num_prefills = 0, num_prefill_tokens = 0;
   std::vector<pkv::WorkItem> work;
   std::vector<pkv::MergeItem> merge;
   std::vector<pkv::ReqInfo> req;

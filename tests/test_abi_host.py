@@ -181,3 +181,57 @@ def test_workspace_size_matches_plan(pk):
     n = pk.Plan.workspace_size(*idx, **a)
     p = pk.Plan().plan(*idx, host_only=True, **a)
     assert p.info()["workspace_bytes"] == n and n % 256 == 0
+
+
+def _mixed_plan(pk, order):
+    """The worked example's three requests (A decode, B 4-token prefill, C 3-token extend) in `order`."""
+    g = json.load(open(os.path.join(GOLDEN, "vllm_worked_example.json")))
+    q_lens = np.diff(g["query_start_loc"]).tolist()
+    rows = [g["block_table"][i] for i in order]
+    seq = [g["seq_lens"][i] for i in order]
+    ql = [q_lens[i] for i in order]
+    indptr, indices, last = pk.block_table_to_csr(rows, seq, g["page_size"])
+    qo = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    p = pk.Plan().plan(qo, indptr, indices, last, num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                       page_size=g["page_size"], mode="mixed", num_sms=152, host_only=True)
+    return g, p, qo
+
+
+@pytest.mark.parametrize("order", [[0, 1, 2], [1, 0, 2], [2, 1, 0]])
+def test_mixed_plan_splits_decode_and_extend_as_printed(pk, order):
+    """Mixed batch: the decode/extend counts and the extend slice's query offsets are the printed ones,
+    whatever the request order (each CTA carries its own token row, so no decode-first reorder)."""
+    g, p, qo = _mixed_plan(pk, order)
+    e = g["expect"]
+    info = p.info()
+    assert info["mode"] == pk._lib.PKV_MODE_MIXED
+    for k in ("num_decodes", "num_decode_tokens", "num_prefills", "num_prefill_tokens"):
+        assert info[k] == e[k]
+    items = p.work_items()
+    nd = info["num_decode_work"]
+    dec, pre = items[:nd], items[nd:]
+    a_pos = order.index(0)  # request A is the decode request
+    assert set(dec[:, 0].tolist()) == {a_pos} and set(dec[:, 5].tolist()) == {int(qo[a_pos])}
+    assert len(dec) == 8  # one CTA per KV head: 128 keys are one chunk
+    assert a_pos not in set(pre[:, 0].tolist())
+    # per KV head, the extend CTAs cover B's and C's rows; in the printed order their query counts
+    # give the prefill slice's qo_indptr
+    for h in range(8):
+        mine = pre[pre[:, 1] == h]
+        got = {int(r[0]): (int(r[5]), int(r[7])) for r in mine}
+        want = {i: (int(qo[i]), int(qo[i + 1] - qo[i])) for i in range(3) if i != a_pos}
+        assert got == want
+    if order == [0, 1, 2]:
+        q_rows = [int(r[7]) for r in sorted(pre[pre[:, 1] == 0].tolist(), key=lambda r: r[5])]
+        assert np.concatenate([[0], np.cumsum(q_rows)]).tolist() == e["prefill_qo_indptr"]
+
+
+def test_mixed_plan_with_only_decodes_needs_no_prefill_support(pk):
+    """A mixed plan whose requests all have one new token is a decode plan (FP8 KV allowed)."""
+    p = pk.Plan().plan([0, 1, 2], [0, 2, 3], [3, 1, 0], [5, 16], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                       page_size=16, mode="mixed", kv_dtype="e4m3", num_sms=152, host_only=True)
+    info = p.info()
+    assert info["num_decode_work"] == info["num_work"] == 2 * 8 and info["num_prefills"] == 0
+    with pytest.raises(pk.PkvError):  # an extend request with an FP8 cache is not supported
+        pk.Plan().plan([0, 1, 3], [0, 2, 3], [3, 1, 0], [5, 16], num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                       page_size=16, mode="mixed", kv_dtype="e4m3", num_sms=152, host_only=True)
