@@ -115,6 +115,16 @@ def visible_range(position: int, window_left: int):
     return lo, position
 
 
+def full_range(kv_len: int):
+    """Inclusive key range [0, kv_len - 1] seen by every query of a non-causal call.
+
+    "SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种形态：ragged 直算与 paged + merge»:
+    the cached-prefix segment is attended with causal=False, because every prefix key lies before
+    every new query, so the whole segment is visible.
+    """
+    return 0, kv_len - 1
+
+
 def gather_logical(pool, pages, kv_len: int, page_size: int):
     """Logical token j of a request lives at pool[pages[j // ps], j % ps]; returns [kv_len, ...]."""
     j = np.arange(kv_len)
@@ -146,12 +156,15 @@ def paged_attention(
     k_scale: float = 1.0,
     v_scale: float = 1.0,
     rows=None,
+    causal: bool = True,
 ):
     """Batched attention over a paged KV cache, float64.
 
     q: [T, Hq, D]; pools: [num_pages, page_size, Hkv, D].  Element formats as in
     ``to_f64``.  ``rows``: optional iterable of token rows of q to compute (the
-    others are left NaN), for sampling large batches.
+    others are left NaN), for sampling large batches.  ``causal=False``: every
+    query sees all kv_len keys of its request (``full_range``); a window is then
+    not allowed and kv_len may be smaller than the number of queries.
 
     Returns (o [T, Hq, D] float64, lse [T, Hq] float64).
     """
@@ -167,6 +180,8 @@ def paged_attention(
     scale = (1.0 / math.sqrt(D)) if (sm_scale is None or sm_scale <= 0) else float(sm_scale)
     if qo_indptr[0] != 0 or np.any(np.diff(qo_indptr) < 0):
         raise ValueError("qo_indptr must start at 0 and be non-decreasing")
+    if not causal and window_left >= 0:
+        raise ValueError("a window needs causal attention")
     wanted = None if rows is None else set(int(r) for r in rows)
 
     o = np.full((T, Hq, D), np.nan)
@@ -181,13 +196,13 @@ def paged_attention(
             continue
         pages = kv_indices[kv_indptr[i] : kv_indptr[i + 1]]
         L = kv_len_of(len(pages), int(last_page_len[i]), page_size)
-        if L < n:
-            raise ValueError(f"request {i}: kv_len {L} < q_len {n}")
+        if (L < n if causal else L == 0):
+            raise ValueError(f"request {i}: kv_len {L} too short for {n} queries")
         K = to_f64(gather_logical(k_pool, pages, L, page_size), kv_format, k_scale)  # [L, Hkv, D]
         V = to_f64(gather_logical(v_pool, pages, L, page_size), kv_format, v_scale)
         Q = to_f64(q[q0:q1], q_format)
         for t in todo:
-            lo, hi = visible_range(query_position(L, n, t), window_left)
+            lo, hi = visible_range(query_position(L, n, t), window_left) if causal else full_range(L)
             for h in range(Hq):
                 kvh = kv_head_of(h, group)
                 o[q0 + t, h], lse[q0 + t, h] = attend(Q[t, h], K[:, kvh], V[:, kvh], lo, hi, scale)

@@ -19,6 +19,9 @@ CHECKS = [
     ("single_key", P.check_single_key),
     ("uniform", P.check_uniform_scores),
     ("merge", P.check_merge_closed_form),
+    ("bruteforce_noncausal", lambda: P.check_bruteforce(causal=False)),
+    ("sdpa_noncausal", lambda: P.check_sdpa(causal=False)),
+    ("prefix_suffix_merge", P.check_prefix_suffix_merge),
 ]
 
 
@@ -52,6 +55,9 @@ MUTATIONS = {
     "last_page_off_by_one": ("kv_len_of", lambda n, last, ps: 0 if n == 0 else (n - 1) * ps + last - 1),
     # gather by offset only within the first page
     "gather_ignores_pages": ("gather_logical", lambda pool, pages, L, ps: pool[np.asarray(pages)[np.zeros(L, dtype=np.int64)], np.arange(L) % ps]),
+    # non-causal range loses its last key, or its first
+    "noncausal_drops_last": ("full_range", lambda L: (0, L - 2)),
+    "noncausal_from_one": ("full_range", lambda L: (1, L - 1)),
     # drop the softmax scale
     "no_scale": ("attend", None),
     # transposed operand: V rows taken from K

@@ -192,7 +192,7 @@ def _small_batch(seed, ps=4, Hq=4, Hkv=2, D=8, lens=((9, 1), (5, 5), (13, 4), (4
                 last_page_len=last, page_size=ps, window_left=window), L, n
 
 
-def _bruteforce(b, L, n, scale):
+def _bruteforce(b, L, n, scale, causal=True):
     """Python loops only: walk each request's pages token by token, softmax with math.exp."""
     q, kp, vp, ps = b["q"], b["k_pool"], b["v_pool"], b["page_size"]
     Hq, D = q.shape[1], q.shape[2]
@@ -212,7 +212,7 @@ def _bruteforce(b, L, n, scale):
             pos = L[i] - n[i] + t
             for h in range(Hq):
                 kh = h // grp
-                js = [j for j in range(L[i]) if j <= pos and (w < 0 or j >= pos - w)]
+                js = [j for j in range(L[i]) if not causal or (j <= pos and (w < 0 or j >= pos - w))]
                 s = [scale * sum(q[row, h, d] * keys[j][kh, d] for d in range(D)) for j in js]
                 mx = max(s)
                 e = [math.exp(x - mx) for x in s]
@@ -223,25 +223,27 @@ def _bruteforce(b, L, n, scale):
     return out, lse
 
 
-def _oracle(b, scale):
+def _oracle(b, scale, causal=True):
     return A.paged_attention(b["q"], b["k_pool"], b["v_pool"], b["qo_indptr"], b["kv_indptr"], b["kv_indices"],
-                             b["last_page_len"], b["page_size"], sm_scale=scale, window_left=b["window_left"])
+                             b["last_page_len"], b["page_size"], sm_scale=scale, window_left=b["window_left"],
+                             causal=causal)
 
 
-def check_bruteforce(window=-1, seed=1):
-    b, L, n = _small_batch(seed, window=window)
+def check_bruteforce(window=-1, seed=1, causal=True):
+    lens = ((9, 1), (5, 5), (13, 4), (4, 2)) if causal else ((9, 1), (3, 5), (13, 4), (4, 2))  # non-causal: L < n allowed
+    b, L, n = _small_batch(seed, window=window, lens=lens)
     scale = 0.37
-    o, lse = _oracle(b, scale)
-    bo, bl = _bruteforce(b, L, n, scale)
+    o, lse = _oracle(b, scale, causal=causal)
+    bo, bl = _bruteforce(b, L, n, scale, causal=causal)
     return np.allclose(o, bo, rtol=0, atol=1e-12) and np.allclose(lse, bl, rtol=0, atol=1e-12)
 
 
-def check_sdpa(window=-1, seed=2):
+def check_sdpa(window=-1, seed=2, causal=True):
     """The library routine the pages' CPU reference uses, in float64, with enable_gqa."""
     b, L, n = _small_batch(seed, ps=4, Hq=8, Hkv=2, D=16, window=window,
                            lens=((17, 3), (6, 6), (30, 1), (8, 0), (12, 7)))
     scale = 0.21
-    o, _ = _oracle(b, scale)
+    o, _ = _oracle(b, scale, causal=causal)
     ps = b["page_size"]
     for i in range(len(L)):
         if n[i] == 0:
@@ -253,7 +255,7 @@ def check_sdpa(window=-1, seed=2):
         qi = torch.from_numpy(b["q"][q0:q1]).transpose(0, 1)
         qpos = torch.arange(L[i] - n[i], L[i]).unsqueeze(1)
         kpos = torch.arange(L[i]).unsqueeze(0)
-        mask = kpos <= qpos
+        mask = kpos <= qpos if causal else torch.ones((n[i], L[i]), dtype=torch.bool)
         if window >= 0:
             mask &= kpos >= qpos - window
         ref = torch.nn.functional.scaled_dot_product_attention(qi, k, v, attn_mask=mask, scale=scale, enable_gqa=True)
@@ -347,8 +349,55 @@ def check_merge_closed_form(seed=7):
     return np.allclose(oe, o, rtol=0, atol=1e-15) and abs(se - s) < 1e-15
 
 
+def check_prefix_suffix_merge(seed=8):
+    """"SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种形态»: causal extend over a cached
+    prefix of p keys plus n new keys = merge of (the n queries over the prefix, causal=False) and (the
+    n queries over the n new keys alone, causal within the segment)."""
+    rng = np.random.default_rng(seed)
+    ps, Hq, Hkv, D = 4, 4, 2, 8
+    for p_len, n in ((7, 3), (1, 6), (12, 1), (5, 5)):
+        L = p_len + n
+        P = (L + ps - 1) // ps + 2
+        kp, vp = rng.normal(size=(P, ps, Hkv, D)), rng.normal(size=(P, ps, Hkv, D))
+        q = rng.normal(size=(n, Hq, D)) * 2
+        pages = rng.permutation(P)[: (L + ps - 1) // ps]
+        full_o, full_s = A.paged_attention(q, kp, vp, [0, n], [0, len(pages)], pages,
+                                           [L - (len(pages) - 1) * ps], ps, sm_scale=0.3)
+        # prefix-only view: the first p keys (same pages, shorter length), every query sees all of them
+        np_pre = (p_len + ps - 1) // ps
+        pre_o, pre_s = A.paged_attention(q, kp, vp, [0, n], [0, np_pre], pages[:np_pre],
+                                         [p_len - (np_pre - 1) * ps], ps, sm_scale=0.3, causal=False)
+        # suffix-only view: the n new keys copied to a fresh pool as their own sequence
+        K = np.stack([kp[pages[j // ps], j % ps] for j in range(p_len, L)])
+        V = np.stack([vp[pages[j // ps], j % ps] for j in range(p_len, L)])
+        suf_o, suf_s = A.paged_attention(q, K[:, None], V[:, None], [0, n], [0, n], np.arange(n), [1],
+                                         1, sm_scale=0.3)
+        mo, ms = A.merge_states(pre_o, pre_s, suf_o, suf_s)
+        if not (np.allclose(mo, full_o, rtol=0, atol=1e-13) and np.allclose(ms, full_s, rtol=0, atol=1e-12)):
+            return False
+    return True
+
+
 def test_bruteforce_tiny():
     assert check_bruteforce()
+
+
+def test_bruteforce_tiny_noncausal():
+    assert check_bruteforce(causal=False)
+
+
+def test_matches_library_sdpa_noncausal():
+    assert check_sdpa(causal=False)
+
+
+def test_prefix_noncausal_merged_with_causal_suffix_equals_causal_extend():
+    assert check_prefix_suffix_merge()
+
+
+def test_noncausal_rejects_a_window():
+    b, L, n = _small_batch(1, window=2)
+    with pytest.raises(ValueError):
+        _oracle(b, 0.5, causal=False)
 
 
 def test_bruteforce_tiny_window():
