@@ -164,7 +164,11 @@ def paged_attention(
     ``to_f64``.  ``rows``: optional iterable of token rows of q to compute (the
     others are left NaN), for sampling large batches.  ``causal=False``: every
     query sees all kv_len keys of its request (``full_range``); a window is then
-    not allowed and kv_len may be smaller than the number of queries.
+    not allowed and kv_len may be smaller than the number of queries.  A
+    non-causal request with kv_len 0 yields the empty state (o = 0, lse = -inf),
+    which ``merge_states`` treats as the identity: in the paged + merge form of
+    extend ("SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种
+    形态»), a request without a cached prefix has an empty paged segment.
 
     Returns (o [T, Hq, D] float64, lse [T, Hq] float64).
     """
@@ -196,8 +200,12 @@ def paged_attention(
             continue
         pages = kv_indices[kv_indptr[i] : kv_indptr[i + 1]]
         L = kv_len_of(len(pages), int(last_page_len[i]), page_size)
-        if (L < n if causal else L == 0):
+        if causal and L < n:
             raise ValueError(f"request {i}: kv_len {L} too short for {n} queries")
+        if L == 0:  # non-causal segment with no keys: the empty state
+            for t in todo:
+                o[q0 + t], lse[q0 + t] = 0.0, -np.inf
+            continue
         K = to_f64(gather_logical(k_pool, pages, L, page_size), kv_format, k_scale)  # [L, Hkv, D]
         V = to_f64(gather_logical(v_pool, pages, L, page_size), kv_format, v_scale)
         Q = to_f64(q[q0:q1], q_format)
@@ -228,6 +236,64 @@ def paged_attention_heads(q_rows, K, V, positions, scale: float, window_left: in
     den = e.sum(axis=-1)
     o = np.einsum("ngl,ld->ngd", e, V) / den[..., None]
     return o, m[..., 0] + np.log(den)
+
+
+def kv_rows_of(kv_indptr, i: int):
+    """Rows [begin, end) of the contiguous K/V tensors that request i owns."""
+    return int(kv_indptr[i]), int(kv_indptr[i + 1])
+
+
+def ragged_attention(q, k, v, qo_indptr, kv_indptr, sm_scale: float | None = None, causal: bool = True,
+                     window_left: int = -1, q_format: str = "float", kv_format: str = "float"):
+    """Batched attention over contiguous ("ragged") K/V, float64.
+
+    "SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种形态»: the
+    ragged form takes this step's K/V as plain tensors, not through the page
+    table.  Request i owns K/V rows kv_indptr[i] .. kv_indptr[i+1]-1 of k / v
+    ([rows, Hkv, D]) in logical order and query rows qo_indptr[i] ..
+    qo_indptr[i+1]-1 of q ([T, Hq, D]).  The visibility rule is the paged one:
+    with causal=True the queries are the last n positions of the request's
+    kv_len keys (bottom-right aligned, optional window); with causal=False every
+    query sees all kv_len keys (kv_len 0 gives the empty state).
+
+    Returns (o [T, Hq, D] float64, lse [T, Hq] float64).
+    """
+    qo_indptr = np.asarray(qo_indptr, dtype=np.int64)
+    kv_indptr = np.asarray(kv_indptr, dtype=np.int64)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if len(kv_indptr) != len(qo_indptr):
+        raise ValueError("qo_indptr and kv_indptr must have the same length")
+    if qo_indptr[0] != 0 or np.any(np.diff(qo_indptr) < 0) or kv_indptr[0] != 0 or np.any(np.diff(kv_indptr) < 0):
+        raise ValueError("indptr arrays must start at 0 and be non-decreasing")
+    if not causal and window_left >= 0:
+        raise ValueError("a window needs causal attention")
+    group = Hq // Hkv
+    scale = (1.0 / math.sqrt(D)) if (sm_scale is None or sm_scale <= 0) else float(sm_scale)
+    o = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    for i in range(len(qo_indptr) - 1):
+        q0, q1 = int(qo_indptr[i]), int(qo_indptr[i + 1])
+        k0, k1 = kv_rows_of(kv_indptr, i)
+        n, L = q1 - q0, k1 - k0
+        if n == 0:
+            continue
+        if causal and L < n:
+            raise ValueError(f"request {i}: kv_len {L} too short for {n} queries")
+        if L == 0:
+            o[q0:q1], lse[q0:q1] = 0.0, -np.inf
+            continue
+        K = to_f64(k[k0:k1], kv_format)
+        V = to_f64(v[k0:k1], kv_format)
+        Q = to_f64(q[q0:q1], q_format)
+        for t in range(n):
+            lo, hi = visible_range(query_position(L, n, t), window_left) if causal else full_range(L)
+            for h in range(Hq):
+                kvh = kv_head_of(h, group)
+                o[q0 + t, h], lse[q0 + t, h] = attend(Q[t, h], K[:, kvh], V[:, kvh], lo, hi, scale)
+    return o, lse
 
 
 # ----------------------------------------------------------------------------------------------

@@ -22,6 +22,9 @@ CHECKS = [
     ("bruteforce_noncausal", lambda: P.check_bruteforce(causal=False)),
     ("sdpa_noncausal", lambda: P.check_sdpa(causal=False)),
     ("prefix_suffix_merge", P.check_prefix_suffix_merge),
+    ("ragged_bruteforce", P.check_ragged_bruteforce),
+    ("ragged_bruteforce_noncausal", lambda: P.check_ragged_bruteforce(causal=False)),
+    ("ragged_sdpa", P.check_ragged_sdpa),
 ]
 
 
@@ -58,6 +61,10 @@ MUTATIONS = {
     # non-causal range loses its last key, or its first
     "noncausal_drops_last": ("full_range", lambda L: (0, L - 2)),
     "noncausal_from_one": ("full_range", lambda L: (1, L - 1)),
+    # ragged K/V rows read one row late (the segment of the next request leaks in)
+    "ragged_rows_shifted": ("kv_rows_of", lambda kv, i: (int(kv[i]) + 1, int(kv[i + 1]) + 1)),
+    # ragged K/V rows taken from the start of the tensor for every request
+    "ragged_rows_from_zero": ("kv_rows_of", lambda kv, i: (0, int(kv[i + 1]) - int(kv[i]))),
     # drop the softmax scale
     "no_scale": ("attend", None),
     # transposed operand: V rows taken from K

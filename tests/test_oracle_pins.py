@@ -355,7 +355,7 @@ def check_prefix_suffix_merge(seed=8):
     n queries over the n new keys alone, causal within the segment)."""
     rng = np.random.default_rng(seed)
     ps, Hq, Hkv, D = 4, 4, 2, 8
-    for p_len, n in ((7, 3), (1, 6), (12, 1), (5, 5)):
+    for p_len, n in ((7, 3), (1, 6), (12, 1), (5, 5), (0, 4)):
         L = p_len + n
         P = (L + ps - 1) // ps + 2
         kp, vp = rng.normal(size=(P, ps, Hkv, D)), rng.normal(size=(P, ps, Hkv, D))
@@ -364,18 +364,93 @@ def check_prefix_suffix_merge(seed=8):
         full_o, full_s = A.paged_attention(q, kp, vp, [0, n], [0, len(pages)], pages,
                                            [L - (len(pages) - 1) * ps], ps, sm_scale=0.3)
         # prefix-only view: the first p keys (same pages, shorter length), every query sees all of them
-        np_pre = (p_len + ps - 1) // ps
+        np_pre = (p_len + ps - 1) // ps  # 0 pages without a prefix: the empty state
         pre_o, pre_s = A.paged_attention(q, kp, vp, [0, n], [0, np_pre], pages[:np_pre],
-                                         [p_len - (np_pre - 1) * ps], ps, sm_scale=0.3, causal=False)
-        # suffix-only view: the n new keys copied to a fresh pool as their own sequence
+                                         [p_len - (np_pre - 1) * ps if np_pre else 0], ps, sm_scale=0.3,
+                                         causal=False)
+        # suffix-only view: the n new keys as contiguous ("ragged") K/V, causal within the segment
         K = np.stack([kp[pages[j // ps], j % ps] for j in range(p_len, L)])
         V = np.stack([vp[pages[j // ps], j % ps] for j in range(p_len, L)])
-        suf_o, suf_s = A.paged_attention(q, K[:, None], V[:, None], [0, n], [0, n], np.arange(n), [1],
-                                         1, sm_scale=0.3)
+        suf_o, suf_s = A.ragged_attention(q, K, V, [0, n], [0, n], sm_scale=0.3)
         mo, ms = A.merge_states(pre_o, pre_s, suf_o, suf_s)
         if not (np.allclose(mo, full_o, rtol=0, atol=1e-13) and np.allclose(ms, full_s, rtol=0, atol=1e-12)):
             return False
     return True
+
+
+def _ragged_batch(seed, lens, Hq=4, Hkv=2, D=8):
+    """Contiguous K/V rows per request (no page table): lens = ((kv_len, q_len), ...)."""
+    rng = np.random.default_rng(seed)
+    L = [a for a, _ in lens]
+    n = [b_ for _, b_ in lens]
+    k = rng.normal(size=(sum(L), Hkv, D))
+    v = rng.normal(size=(sum(L), Hkv, D))
+    q = rng.normal(size=(sum(n), Hq, D)) * 2
+    return q, k, v, np.concatenate([[0], np.cumsum(n)]), np.concatenate([[0], np.cumsum(L)]), L, n
+
+
+def check_ragged_bruteforce(seed=11, causal=True):
+    """Python loops over each request's contiguous rows; a request with no keys must give (0, -inf)."""
+    lens = ((6, 6), (9, 2), (3, 3), (5, 1)) if causal else ((6, 6), (2, 5), (0, 3), (5, 1))
+    q, k, v, qo, kv, L, n = _ragged_batch(seed, lens)
+    scale = 0.41
+    o, lse = A.ragged_attention(q, k, v, qo, kv, sm_scale=scale, causal=causal)
+    Hq, D = q.shape[1], q.shape[2]
+    grp = Hq // k.shape[1]
+    for i in range(len(L)):
+        for t in range(n[i]):
+            row = qo[i] + t
+            pos = L[i] - n[i] + t
+            js = [j for j in range(L[i]) if not causal or j <= pos]
+            for h in range(Hq):
+                if not js:
+                    if not (np.all(o[row, h] == 0.0) and lse[row, h] == -math.inf):
+                        return False
+                    continue
+                s = [scale * math.fsum(q[row, h, d] * k[kv[i] + j, h // grp, d] for d in range(D)) for j in js]
+                mx = max(s)
+                e = [math.exp(x - mx) for x in s]
+                den = math.fsum(e)
+                for d in range(D):
+                    if abs(o[row, h, d] - math.fsum(e[a] * v[kv[i] + j, h // grp, d] for a, j in enumerate(js)) / den) > 1e-12:
+                        return False
+                if abs(lse[row, h] - (mx + math.log(den))) > 1e-12:
+                    return False
+    return True
+
+
+def check_ragged_sdpa(seed=12):
+    """Causal self-attention over a fresh segment (n == kv_len) is SDPA's is_causal form."""
+    q, k, v, qo, kv, L, n = _ragged_batch(seed, ((7, 7), (1, 1), (12, 12)), Hq=8, Hkv=2, D=16)
+    o, _ = A.ragged_attention(q, k, v, qo, kv, sm_scale=0.23)
+    for i in range(len(L)):
+        qi = torch.from_numpy(q[qo[i]:qo[i + 1]]).transpose(0, 1)
+        ki = torch.from_numpy(k[kv[i]:kv[i + 1]]).transpose(0, 1)
+        vi = torch.from_numpy(v[kv[i]:kv[i + 1]]).transpose(0, 1)
+        ref = torch.nn.functional.scaled_dot_product_attention(qi, ki, vi, is_causal=True, scale=0.23, enable_gqa=True)
+        if not np.allclose(o[qo[i]:qo[i + 1]], ref.transpose(0, 1).numpy(), rtol=0, atol=1e-12):
+            return False
+    return True
+
+
+def test_ragged_bruteforce_causal():
+    assert check_ragged_bruteforce()
+
+
+def test_ragged_bruteforce_noncausal_and_empty_segment():
+    assert check_ragged_bruteforce(causal=False)
+
+
+def test_ragged_matches_library_sdpa_is_causal():
+    assert check_ragged_sdpa()
+
+
+def test_noncausal_paged_segment_without_keys_is_the_empty_state():
+    b, L, n = _small_batch(13, lens=((5, 2), (0, 3), (4, 4)))
+    o, lse = _oracle(b, 0.5, causal=False)
+    r = slice(b["qo_indptr"][1], b["qo_indptr"][2])
+    assert np.all(o[r] == 0.0) and np.all(lse[r] == -np.inf)
+    assert np.all(np.isfinite(lse[: b["qo_indptr"][1]]))
 
 
 def test_bruteforce_tiny():
