@@ -57,12 +57,16 @@ typedef enum {
 typedef enum {
   PKV_MODE_DECODE = 0,  /* one new token per request (qo_indptr[i+1] - qo_indptr[i] in {0, 1}) */
   PKV_MODE_PREFILL = 1, /* any number of new tokens per request (prefill / prefix-cached extend) */
-  PKV_MODE_MIXED = 2    /* both in one batch: requests with one new token are planned for the
+  PKV_MODE_MIXED = 2,   /* both in one batch: requests with one new token are planned for the
                          * decode kernel, requests with more for the prefill kernel, and the two
                          * runs write their rows of one output (the decode / prefill-extend split
                          * of "vLLM Attention 后端与 FlashInfer 元数据", sections «为什么先把 Decode 移到前面»
                          * and «FlashInfer Builder 的结果»).  Requests may come in any order: every
                          * CTA carries its own token row, so no decode-first reordering is needed. */
+  PKV_MODE_RAGGED = 3   /* prefill / extend over CONTIGUOUS K/V tensors instead of the paged pool
+                         * (the ragged form of "SGLang 源码完全拆解(八)：Attention Backend", section
+                         * «extend 的两种形态»): kv_indptr holds TOKEN offsets into k / v, kv_indices,
+                         * last_page_len and page_size are ignored; run with pkv_attn_ragged_run. */
 } pkv_mode;
 
 /* Device error codes a kernel may record (read with pkv_device_error). */
@@ -150,7 +154,9 @@ int pkv_kv_store(const void* k, const void* v, const int64_t* slot_mapping, int6
  * window_left = w >= 0 only to keys j >= P - w ("SGLang 源码完全拆解(八)：Attention Backend",
  * section «mask 从哪里来»).  Query head h reads KV head h / (num_qo_heads / num_kv_heads).
  * Checked: L_i >= n_i; L_i == 0 only if n_i == 0 (invariants 3-6 of "vLLM 源码完全拆解（六）：
- * Attention Backend", section «九条必须成立的不变量»).
+ * Attention Backend", section «九条必须成立的不变量»); with causal == 0 only kv_indptr's order.
+ * PKV_MODE_RAGGED: kv_indptr[i] .. kv_indptr[i+1]-1 are the rows of the contiguous k / v tensors
+ * that request i owns (L_i = kv_indptr[i+1] - kv_indptr[i]); no page table is involved.
  */
 typedef struct pkv_plan_args {
   int32_t batch_size;
@@ -163,7 +169,11 @@ typedef struct pkv_plan_args {
   int32_t head_dim;      /* 64 or 128 (decode); 128 (prefill)                                */
   int32_t page_size;     /* >= 1                                                             */
   int32_t mode;          /* pkv_mode                                                         */
-  int32_t causal;        /* must be 1                                                        */
+  int32_t causal;        /* 1: bottom-right-aligned causal mask (every mode).  0: every query */
+                         /* of request i sees all L_i keys (PKV_MODE_PREFILL / _RAGGED only; */
+                         /* window_left must be -1; L_i < n_i is allowed and L_i == 0 gives  */
+                         /* the empty state o = 0, lse = -inf) -- the cached-prefix segment  */
+                         /* of the paged + merge extend, attended with causal=False          */
   int32_t window_left;   /* -1: no window; w >= 0 keeps keys P - w .. P                       */
   float sm_scale;        /* <= 0 selects 1 / sqrt(head_dim)                                  */
   int32_t q_dtype;       /* PKV_BF16                                                         */
@@ -227,6 +237,36 @@ int pkv_attn_decode_run(const pkv_plan* plan, const void* q, const pkv_cache* ca
                         void* stream);
 int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
                          void* stream);
+
+/*
+ * pkv_attn_ragged_run: attention of a PKV_MODE_RAGGED plan, K/V read from contiguous tensors (the
+ * ragged wrapper's forward of "SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种
+ * 形态»: the new tokens' K/V straight from this step's k / v, not through the page table).
+ *   q     device bf16 [total_tokens, num_qo_heads, 128], contiguous.
+ *   k, v  device bf16 [kv_indptr[batch_size], num_kv_heads, 128], contiguous, 16-byte aligned.
+ *   o, lse as for pkv_attn_prefill_run (o bf16; lse natural log, NULL allowed).
+ * Same kernel, visibility rule and errors as pkv_attn_prefill_run.
+ */
+int pkv_attn_ragged_run(const pkv_plan* plan, const void* q, const void* k, const void* v, void* o, float* lse,
+                        void* stream);
+
+/*
+ * pkv_merge_state: merge two attention states of the same rows ("SGLang 源码完全拆解(八)：Attention
+ * Backend", section «extend 的两种形态»: o = (o_a e^(s_a - m) + o_b e^(s_b - m)) / (e^(s_a - m) +
+ * e^(s_b - m)), m = max(s_a, s_b); the merged log-sum-exp is m + ln(e^(s_a - m) + e^(s_b - m));
+ * "vLLM 源码完全拆解（六）：Attention Backend", section «Cascade Attention 把共享前缀只算一次»: the
+ * shared-prefix and suffix outputs are combined by their LSE weights, never added).
+ *   o_a, o_b, o   device bf16 [num_states, head_dim] (a state = one (token row, query head) pair;
+ *                 [tokens, heads, head_dim] contiguous is the same thing), 16-byte aligned.
+ *   lse_a, lse_b  device float32 [num_states], natural log (as the runs export it).  A state with
+ *                 lse = -inf is empty and contributes nothing; two empty states give o = 0,
+ *                 lse = -inf.
+ *   lse           device float32 [num_states] or NULL.
+ * o may alias o_a or o_b and lse may alias lse_a or lse_b (in-place merge).  head_dim 64 or 128.
+ * Arithmetic in float32, output rounded to bf16 once.
+ */
+int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
+                    int64_t num_states, int32_t head_dim, void* stream);
 
 /*
  * pkv_attn_decode_run_noalloc: pkv_attn_decode_run for callers that cannot allocate device memory.

@@ -12,6 +12,15 @@ Typical use (plan once per batch, run once per layer):
     plan.plan(qo_indptr, kv_indptr, kv_indices, last_page_len,
               num_qo_heads=32, num_kv_heads=8, head_dim=128, page_size=16, mode="decode")
     out, lse = plan.run(q, cache, return_lse=True)
+
+Prefix-cached extend in the paged + merge form (new tokens' K/V read directly, the cached prefix
+through the page table with every prefix key visible, the two states merged by their LSE):
+
+    rag = Plan().plan(qo_indptr, qo_indptr, None, None, ..., mode="ragged")       # causal
+    pre = Plan().plan(qo_indptr, pre_indptr, pre_indices, pre_last, ..., mode="prefill", causal=False)
+    o1, s1 = rag.run_ragged(q, k_new, v_new, return_lse=True)
+    o2, s2 = pre.run(q, cache, return_lse=True)
+    out, lse = merge_state(o1, s1, o2, s2)
 """
 
 from __future__ import annotations
@@ -25,7 +34,7 @@ from . import _lib
 from ._lib import PkvError, check, lib
 
 __all__ = [
-    "KVCache", "Plan", "PkvError", "kv_store", "device_error", "block_table_to_csr",
+    "KVCache", "Plan", "PkvError", "kv_store", "merge_state", "device_error", "block_table_to_csr",
     "token_table_to_page_table", "library_path",
 ]
 
@@ -139,33 +148,39 @@ class Plan:
 
     @staticmethod
     def _args(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads, head_dim, page_size,
-              mode, window_left, sm_scale, kv_dtype, max_splits, num_sms):
-        arrs = [_i32(qo_indptr), _i32(kv_indptr), _i32(kv_indices), _i32(last_page_len)]
-        B = len(arrs[3])
+              mode, window_left, sm_scale, kv_dtype, max_splits, num_sms, causal=True):
+        # ragged plans have no page table: kv_indices / last_page_len may be None
+        arrs = [_i32(qo_indptr), _i32(kv_indptr), _i32([] if kv_indices is None else kv_indices),
+                _i32([] if last_page_len is None else last_page_len)]
+        B = len(arrs[0]) - 1
         m = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL,
-             "mixed": _lib.PKV_MODE_MIXED}[mode]
+             "mixed": _lib.PKV_MODE_MIXED, "ragged": _lib.PKV_MODE_RAGGED}[mode]
         kd = {"bf16": _lib.PKV_BF16, "e4m3": _lib.PKV_FP8_E4M3, "fp8": _lib.PKV_FP8_E4M3}[kv_dtype]
         a = _lib.pkv_plan_args(B, _ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(arrs[3]), num_qo_heads,
-                               num_kv_heads, head_dim, page_size, m, 1, window_left, float(sm_scale),
-                               _lib.PKV_BF16, kd, max_splits, num_sms)
+                               num_kv_heads, head_dim, page_size, m, 1 if causal else 0, window_left,
+                               float(sm_scale), _lib.PKV_BF16, kd, max_splits, num_sms)
         return a, arrs
 
     @staticmethod
     def workspace_size(qo_indptr, kv_indptr, kv_indices, last_page_len, *, num_qo_heads, num_kv_heads, head_dim,
-                       page_size, mode="decode", window_left=-1, sm_scale=0.0, kv_dtype="bf16", max_splits=0,
-                       num_sms=0) -> int:
+                       page_size=1, mode="decode", window_left=-1, sm_scale=0.0, kv_dtype="bf16", max_splits=0,
+                       num_sms=0, causal=True) -> int:
         a, keep = Plan._args(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads,
-                             head_dim, page_size, mode, window_left, sm_scale, kv_dtype, max_splits, num_sms)
+                             head_dim, page_size, mode, window_left, sm_scale, kv_dtype, max_splits, num_sms, causal)
         n = C.c_size_t(0)
         check(lib().pkv_plan_workspace_size(C.byref(a), C.byref(n)))
         return int(n.value)
 
     def plan(self, qo_indptr, kv_indptr, kv_indices, last_page_len, *, num_qo_heads, num_kv_heads, head_dim,
-             page_size, mode="decode", window_left=-1, sm_scale=0.0, kv_dtype="bf16", max_splits=0, num_sms=0,
-             workspace: torch.Tensor | None = None, host_only: bool = False, stream=None) -> "Plan":
-        """Plan a batch.  Host int arrays in; the binding keeps a device workspace (grown on demand)."""
+             page_size=1, mode="decode", window_left=-1, sm_scale=0.0, kv_dtype="bf16", max_splits=0, num_sms=0,
+             causal=True, workspace: torch.Tensor | None = None, host_only: bool = False, stream=None) -> "Plan":
+        """Plan a batch.  Host int arrays in; the binding keeps a device workspace (grown on demand).
+
+        mode "ragged": kv_indptr holds row offsets into contiguous k / v tensors (run with
+        run_ragged); kv_indices, last_page_len and page_size are ignored.  causal=False: every query
+        sees all keys of its request (prefill / ragged plans)."""
         a, keep = self._args(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads, head_dim,
-                             page_size, mode, window_left, sm_scale, kv_dtype, max_splits, num_sms)
+                             page_size, mode, window_left, sm_scale, kv_dtype, max_splits, num_sms, causal)
         if host_only:
             check(lib().pkv_attn_plan(self._h, C.byref(a), None, 0, None))
         else:
@@ -187,6 +202,8 @@ class Plan:
         self.num_qo_heads = num_qo_heads
         self.head_dim = head_dim
         self.total_tokens = int(keep[0][-1]) if len(keep[0]) else 0
+        self.kv_rows = int(keep[1][-1]) if (mode == "ragged" and len(keep[1])) else 0
+        self.num_kv_heads = num_kv_heads
         self._keep = keep
         return self
 
@@ -201,9 +218,7 @@ class Plan:
         check(lib().pkv_plan_work_items(self._h, _ptr(out), out.size))
         return out[: n * 8].reshape(n, 8)
 
-    def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            return_lse: bool = False, stream=None):
-        """Attention for every planned token row; q is [total_tokens, num_qo_heads, head_dim] bf16."""
+    def _outputs(self, q, out, lse, return_lse):
         if q.dtype != torch.bfloat16 or not q.is_contiguous():
             raise ValueError("q must be a contiguous bf16 tensor")
         if tuple(q.shape) != (self.total_tokens, self.num_qo_heads, self.head_dim):
@@ -212,6 +227,29 @@ class Plan:
             out = torch.empty_like(q)
         if (return_lse or lse is not None) and lse is None:
             lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        return out, lse
+
+    def run_ragged(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor | None = None,
+                   lse: torch.Tensor | None = None, return_lse: bool = False, stream=None):
+        """Attention of a "ragged" plan: k, v are contiguous bf16 [kv_indptr[-1], num_kv_heads, head_dim]."""
+        if self.mode != "ragged":
+            raise ValueError("run_ragged needs a plan made with mode='ragged'")
+        for name, t in (("k", k), ("v", v)):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bf16 tensor")
+            if tuple(t.shape) != (self.kv_rows, self.num_kv_heads, self.head_dim):
+                raise ValueError(f"{name} must be [{self.kv_rows}, {self.num_kv_heads}, {self.head_dim}]")
+        out, lse = self._outputs(q, out, lse, return_lse)
+        check(lib().pkv_attn_ragged_run(self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                        lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
+        return (out, lse) if (return_lse or lse is not None) else out
+
+    def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+            return_lse: bool = False, stream=None):
+        """Attention for every planned token row; q is [total_tokens, num_qo_heads, head_dim] bf16."""
+        if self.mode == "ragged":
+            raise ValueError("a ragged plan runs with run_ragged(q, k, v)")
+        out, lse = self._outputs(q, out, lse, return_lse)
         if self.mode == "decode":
             fns = [lib().pkv_attn_decode_run]
         elif self.mode == "mixed":  # one-token rows on the decode kernel, the rest on the prefill kernel
@@ -222,6 +260,29 @@ class Plan:
             check(fn(self._h, q.data_ptr(), C.byref(cache.struct), out.data_ptr(),
                      lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
         return (out, lse) if (return_lse or lse is not None) else out
+
+
+def merge_state(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor, lse_b: torch.Tensor,
+                out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None, stream=None):
+    """Merge two attention states of the same rows by their log-sum-exp (natural log).
+
+    o_*: bf16 [..., head_dim] contiguous; lse_*: float32 with o's shape minus the last dimension.
+    out / lse_out may be o_a / lse_a (in place).  Returns (out, lse_out)."""
+    if o_a.shape != o_b.shape or lse_a.shape != lse_b.shape or tuple(lse_a.shape) != tuple(o_a.shape[:-1]):
+        raise ValueError("o_a, o_b must share a shape and lse_a, lse_b must be that shape without head_dim")
+    for t in (o_a, o_b):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("o_a and o_b must be contiguous bf16 tensors")
+    for t in (lse_a, lse_b):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("lse_a and lse_b must be contiguous float32 tensors")
+    if out is None:
+        out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    check(lib().pkv_merge_state(o_a.data_ptr(), lse_a.data_ptr(), o_b.data_ptr(), lse_b.data_ptr(), out.data_ptr(),
+                                lse_out.data_ptr(), lse_a.numel(), o_a.shape[-1], _stream_ptr(stream)))
+    return out, lse_out
 
 
 def block_table_to_csr(block_table, seq_lens, page_size: int):

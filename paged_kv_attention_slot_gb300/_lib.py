@@ -25,6 +25,7 @@ PKV_FP8_E4M3 = 1
 PKV_MODE_DECODE = 0
 PKV_MODE_PREFILL = 1
 PKV_MODE_MIXED = 2
+PKV_MODE_RAGGED = 3
 
 STATUS_NAMES = {0: "PKV_OK", -1: "PKV_EINVAL", -2: "PKV_EUNSUPPORTED", -3: "PKV_EWORKSPACE", -4: "PKV_ECUDA",
                 -5: "PKV_EDEVICE"}
@@ -108,6 +109,9 @@ _SIGS = {
     "pkv_attn_decode_run": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_attn_decode_run_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_attn_prefill_run": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
+    "pkv_attn_ragged_run": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "pkv_merge_state": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
+                                  C.c_int32, C.c_void_p]),
     "pkv_last_error": (C.c_char_p, []),
     "pkv_device_error": (C.c_int, [_i32p, C.c_int32, C.c_void_p]),
     "pkv_plan_info_get": (C.c_int, [C.c_void_p, C.POINTER(pkv_plan_info)]),

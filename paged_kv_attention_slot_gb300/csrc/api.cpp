@@ -109,17 +109,24 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   if (!a) return fail(PKV_EINVAL, "args is NULL");
   const int32_t B = a->batch_size;
   if (B < 0) return fail(PKV_EINVAL, "batch_size < 0");
-  if (B > 0 && (!a->qo_indptr || !a->kv_indptr || !a->last_page_len))
-    return fail(PKV_EINVAL, "qo_indptr, kv_indptr and last_page_len must be non-NULL");
+  if (a->mode != PKV_MODE_DECODE && a->mode != PKV_MODE_PREFILL && a->mode != PKV_MODE_MIXED &&
+      a->mode != PKV_MODE_RAGGED)
+    return fail(PKV_EINVAL, "unknown mode");
+  const bool ragged = a->mode == PKV_MODE_RAGGED;  // K/V rows of contiguous tensors, no page table
+  if (B > 0 && (!a->qo_indptr || !a->kv_indptr || (!ragged && !a->last_page_len)))
+    return fail(PKV_EINVAL, ragged ? "qo_indptr and kv_indptr must be non-NULL"
+                                   : "qo_indptr, kv_indptr and last_page_len must be non-NULL");
   if (a->num_qo_heads <= 0 || a->num_kv_heads <= 0) return fail(PKV_EINVAL, "head counts must be positive");
   if (a->num_qo_heads % a->num_kv_heads)
     return fail(PKV_EINVAL, "num_qo_heads must be a multiple of num_kv_heads");
   if (a->head_dim != 64 && a->head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
-  if (a->page_size < 1) return fail(PKV_EINVAL, "page_size must be >= 1");
-  if (a->mode != PKV_MODE_DECODE && a->mode != PKV_MODE_PREFILL && a->mode != PKV_MODE_MIXED)
-    return fail(PKV_EINVAL, "unknown mode");
-  if (a->causal != 1) return fail(PKV_EUNSUPPORTED, "only causal (bottom-right aligned) attention is implemented");
+  if (!ragged && a->page_size < 1) return fail(PKV_EINVAL, "page_size must be >= 1");
+  if (a->causal != 0 && a->causal != 1) return fail(PKV_EINVAL, "causal must be 0 or 1");
   if (a->window_left < -1) return fail(PKV_EINVAL, "window_left must be -1 or >= 0");
+  const bool causal = a->causal == 1;
+  if (!causal && a->mode != PKV_MODE_PREFILL && !ragged)
+    return fail(PKV_EINVAL, "causal == 0 needs a PKV_MODE_PREFILL or PKV_MODE_RAGGED plan");
+  if (!causal && a->window_left >= 0) return fail(PKV_EINVAL, "a sliding window needs causal == 1");
   if (!(std::isfinite(a->sm_scale))) return fail(PKV_EINVAL, "sm_scale is not finite");
   if (a->q_dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "q_dtype must be PKV_BF16");
   if (a->kv_dtype != PKV_BF16 && a->kv_dtype != PKV_FP8_E4M3) return fail(PKV_EINVAL, "unknown kv_dtype");
@@ -128,7 +135,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   if (a->max_splits < 0) return fail(PKV_EINVAL, "max_splits < 0");
   const int32_t G = a->num_qo_heads / a->num_kv_heads;
   // requests with more than one new token go to the prefill kernel (all of them in prefill mode)
-  bool any_extend = a->mode == PKV_MODE_PREFILL;
+  bool any_extend = a->mode == PKV_MODE_PREFILL || ragged;
   if (a->mode == PKV_MODE_MIXED)
     for (int32_t i = 0; i < B && !any_extend; ++i) any_extend = a->qo_indptr[i + 1] - a->qo_indptr[i] > 1;
   if (any_extend) {
@@ -143,8 +150,9 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     if (a->qo_indptr[0] != 0) return fail(PKV_EINVAL, "qo_indptr[0] must be 0");
     if (a->kv_indptr[0] != 0) return fail(PKV_EINVAL, "kv_indptr[0] must be 0");
   }
+  // paged: kv_indptr counts pages of kv_indices; ragged: it counts rows of the k / v tensors
   int64_t nnz = B > 0 ? a->kv_indptr[B] : 0;
-  if (nnz > 0 && !a->kv_indices) return fail(PKV_EINVAL, "kv_indices is NULL");
+  if (!ragged && nnz > 0 && !a->kv_indices) return fail(PKV_EINVAL, "kv_indices is NULL");
 
   P->req.assign(B, ReqInfo{});
   P->max_page_id = -1;
@@ -155,22 +163,26 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     if (n < 0) return fail(PKV_EINVAL, "qo_indptr must be non-decreasing (request " + std::to_string(i) + ")");
     if (np < 0) return fail(PKV_EINVAL, "kv_indptr must be non-decreasing (request " + std::to_string(i) + ")");
     int64_t L = 0;
-    if (np > 0) {
+    if (ragged) {
+      L = np;
+    } else if (np > 0) {
       const int32_t last = a->last_page_len[i];
       if (last < 1 || last > a->page_size)
         return fail(PKV_EINVAL, "last_page_len must be in [1, page_size] (request " + std::to_string(i) + ")");
       L = (np - 1) * (int64_t)a->page_size + last;
     }
     if (L > INT32_MAX) return fail(PKV_EUNSUPPORTED, "KV length exceeds 2^31-1");
-    if (L < n)
+    if (causal && L < n)
       return fail(PKV_EINVAL, "kv_len < q_len (request " + std::to_string(i) + "): seq_len - query_len must be the cached context");
     if (a->mode == PKV_MODE_DECODE && n > 1)
       return fail(PKV_EINVAL, "decode mode allows at most one new token per request (request " + std::to_string(i) + ")");
     P->req[i] = ReqInfo{a->kv_indptr[i], (int32_t)L, a->qo_indptr[i], (int32_t)n};
   }
-  P->indices.resize(nnz);
-  if (nnz) std::memcpy(P->indices.data(), a->kv_indices, nnz * sizeof(int32_t));
-  {
+  P->indices.resize(ragged ? 0 : nnz);
+  if (!ragged && nnz) std::memcpy(P->indices.data(), a->kv_indices, nnz * sizeof(int32_t));
+  if (ragged) {
+    P->max_page_id = nnz - 1;  // the largest K/V row the plan reads
+  } else {
     int32_t mn = 0, mx = -1;
     const int32_t* ix = a->kv_indices;
     if (nnz) mn = mx = ix[0];
@@ -191,7 +203,9 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   P->Hq = a->num_qo_heads;
   P->Hkv = a->num_kv_heads;
   P->D = a->head_dim;
-  P->ps = a->page_size;
+  P->ps = ragged ? 1 : a->page_size;
+  P->causal = causal;
+  P->ragged = ragged;
   P->window_left = a->window_left;
   P->kv_dtype = a->kv_dtype;
   P->q_dtype = a->q_dtype;
@@ -207,7 +221,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
 
   // decode rows: every request in decode mode, the one-token requests in mixed mode
   const bool plan_decode = a->mode == PKV_MODE_DECODE || a->mode == PKV_MODE_MIXED;
-  const bool plan_prefill = a->mode == PKV_MODE_PREFILL || a->mode == PKV_MODE_MIXED;
+  const bool plan_prefill = a->mode == PKV_MODE_PREFILL || a->mode == PKV_MODE_MIXED || ragged;
   if (plan_decode) {
     const int32_t groups = (G + pkv::kDecodeRows - 1) / pkv::kDecodeRows;
     struct Unit { int32_t req, lo, hi; };
@@ -323,8 +337,9 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
       P->num_prefill_tokens += r.q_len;
       for (int32_t t0 = 0; t0 < r.q_len; t0 += tok_per_tile) {
         const int32_t rows = std::min(tok_per_tile, r.q_len - t0);
+        // causal: keys up to the last row's position (bottom-right aligned); otherwise all L keys
         const int32_t pos0 = r.kv_len - r.q_len + t0;
-        const int32_t last_pos = pos0 + rows - 1;
+        const int32_t last_pos = causal ? pos0 + rows - 1 : r.kv_len - 1;
         const int32_t lo = a->window_left >= 0 ? std::max(0, pos0 - a->window_left) : 0;
         P->kv_tokens += (int64_t)(last_pos + 1 - lo);
         for (int32_t h = 0; h < a->num_kv_heads; ++h) {
@@ -426,6 +441,8 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
   p.group = P->Hq / P->Hkv;
   p.head_dim = P->D;
   p.window_left = P->window_left;
+  p.noncausal = P->causal ? 0 : 1;
+  p.ragged_kv = P->ragged ? 1 : 0;
   const float log2e = 1.4426950408889634f;
   p.scale_log2 = P->sm_scale * log2e * (c->dtype == PKV_FP8_E4M3 ? c->k_scale : 1.0f);
   p.out_scale = c->dtype == PKV_FP8_E4M3 ? c->v_scale : 1.0f;
@@ -437,9 +454,10 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
 int check_run(const pkv_plan* P, int mode, const void* q, const pkv_cache* c, void* o) {
   if (!P || !P->valid) return fail(PKV_EINVAL, "plan is NULL or has not been planned");
   if (!P->ws) return fail(PKV_EINVAL, "the plan is host-only (planned without a workspace)");
-  if (P->mode != mode && P->mode != PKV_MODE_MIXED)
-    return fail(PKV_EINVAL, mode == PKV_MODE_DECODE ? "decode_run needs a PKV_MODE_DECODE or PKV_MODE_MIXED plan"
-                                                    : "prefill_run needs a PKV_MODE_PREFILL or PKV_MODE_MIXED plan");
+  if (mode == PKV_MODE_RAGGED ? P->mode != PKV_MODE_RAGGED : (P->mode != mode && P->mode != PKV_MODE_MIXED))
+    return fail(PKV_EINVAL, mode == PKV_MODE_DECODE    ? "decode_run needs a PKV_MODE_DECODE or PKV_MODE_MIXED plan"
+                            : mode == PKV_MODE_RAGGED ? "ragged_run needs a PKV_MODE_RAGGED plan"
+                                                      : "prefill_run needs a PKV_MODE_PREFILL or PKV_MODE_MIXED plan");
   int st = check_cache(P, c);
   if (st != PKV_OK) return st;
   if (P->total_tokens > 0 && (!q || !o)) return fail(PKV_EINVAL, "q and o must be non-NULL");
@@ -599,9 +617,14 @@ int pkv_attn_decode_run(const pkv_plan* plan, const void* q, const pkv_cache* ca
   return PKV_OK;
 }
 
-int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
-                         void* stream) {
-  int st = check_run(plan, PKV_MODE_PREFILL, q, cache, o);
+}  // extern "C"
+
+namespace {
+// The prefill kernel over the plan's prefill items; `cache` is the pool (paged) or a one-token-page
+// view of the contiguous K/V tensors (ragged).
+int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* cache, void* o, float* lse,
+                void* stream) {
+  int st = check_run(plan, mode, q, cache, o);
   if (st != PKV_OK) return st;
   const int64_t first = plan->num_decode_work, count = (int64_t)plan->work.size() - first;
   if (count == 0) return PKV_OK;
@@ -643,6 +666,48 @@ int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* c
   }
   pkv::RunParams p = make_params(plan, q, cache, o, lse, first, count);
   PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
+  return PKV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                         void* stream) {
+  return run_prefill(plan, PKV_MODE_PREFILL, q, cache, o, lse, stream);
+}
+
+int pkv_attn_ragged_run(const pkv_plan* plan, const void* q, const void* k, const void* v, void* o, float* lse,
+                        void* stream) {
+  if (!plan || !plan->valid) return fail(PKV_EINVAL, "plan is NULL or has not been planned");
+  if (plan->mode != PKV_MODE_RAGGED) return fail(PKV_EINVAL, "ragged_run needs a PKV_MODE_RAGGED plan");
+  if (plan->work.empty()) return PKV_OK;  // no request has a new token
+  if (plan->max_page_id >= 0 && (!k || !v)) return fail(PKV_EINVAL, "k and v must be non-NULL");
+  // [rows, Hkv, D] contiguous tensors seen as a pool of one-token pages
+  pkv_cache view{};
+  view.k = const_cast<void*>(k ? k : q);
+  view.v = const_cast<void*>(v ? v : q);
+  view.num_pages = plan->max_page_id + 1;
+  view.page_size = 1;
+  view.num_kv_heads = plan->Hkv;
+  view.head_dim = plan->D;
+  view.dtype = PKV_BF16;
+  view.stride_page = view.stride_token = (int64_t)plan->Hkv * plan->D;
+  view.stride_head = plan->D;
+  view.k_scale = view.v_scale = 1.f;
+  if (view.num_pages == 0) view.num_pages = 1;  // no rows read; keeps the tensor maps well formed
+  return run_prefill(plan, PKV_MODE_RAGGED, q, &view, o, lse, stream);
+}
+
+int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
+                    int64_t num_states, int32_t head_dim, void* stream) {
+  if (num_states < 0) return fail(PKV_EINVAL, "num_states < 0");
+  if (head_dim != 64 && head_dim != 128) return fail(PKV_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (num_states == 0) return PKV_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o) return fail(PKV_EINVAL, "NULL pointer argument");
+  if (((uintptr_t)o_a | (uintptr_t)o_b | (uintptr_t)o) & 15) return fail(PKV_EINVAL, "o_a, o_b and o must be 16-byte aligned");
+  PKV_CUDA(pkv::launch_merge_state(o_a, lse_a, o_b, lse_b, o, lse, num_states, head_dim, (cudaStream_t)stream),
+           "merge launch");
   return PKV_OK;
 }
 

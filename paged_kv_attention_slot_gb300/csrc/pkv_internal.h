@@ -80,6 +80,8 @@ struct RunParams {
   int32_t group;       // num_qo_heads / num_kv_heads
   int32_t head_dim;
   int32_t window_left;
+  int32_t noncausal;   // prefill: 1 = every query sees all of its request's keys (0 = causal)
+  int32_t ragged_kv;   // prefill: 1 = key j of request i is row page_base + j of the pools (no page table)
   float scale_log2;    // sm_scale * log2(e) (* k_scale for FP8 KV)
   float out_scale;     // 1, or v_scale for FP8 KV
   int64_t num_work;
@@ -94,6 +96,8 @@ int decode_ctas_per_sm(int kv_dtype, int head_dim, int group);  // resident deco
 cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v,
                            int64_t total_tokens, cudaStream_t s);
 int prefill_supported(const char** why);
+cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o,
+                               float* lse, int64_t num_states, int head_dim, cudaStream_t s);
 
 cudaError_t read_device_error(int32_t* code, int reset, cudaStream_t s);
 
@@ -106,6 +110,8 @@ int set_last_error(int code, const char* msg);
 struct pkv_plan {
   bool valid = false;
   int32_t mode = 0, batch = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, window_left = -1, kv_dtype = 0, q_dtype = 0;
+  bool causal = true;   // false: every query sees all keys of its request (prefill / ragged plans)
+  bool ragged = false;  // PKV_MODE_RAGGED: request i reads rows kv_indptr[i].. of contiguous K/V; max_page_id = last row
   float sm_scale = 0.f;
   int64_t total_tokens = 0, max_page_id = -1, kv_tokens = 0, kv_chunk = 0, num_partials = 0;
   int64_t num_decode_work = 0;  // the decode kernel's items come first in `work`, the prefill kernel's after

@@ -108,6 +108,24 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   (void)tk;
   (void)tv;
 
+  if (nkt == 0) {
+    // a non-causal segment without keys: the empty state (o = 0, lse = -inf) for every row.
+    // Thread i writes half (i & 1) of row i / 2 of the two tiles.
+    const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int x = r >> 7, rr = r & (ROWS - 1);
+    const int t = x * T + rr / G, g = rr % G;
+    if (t < w.q_rows) {
+      const int64_t row = (int64_t)(w.q_row + t);
+      const int head = w.kv_head * G + g;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D +
+                                            half * (D / 2));
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (half == 0 && p.lse) p.lse[row * p.num_qo_heads + head] = -INFINITY;
+    }
+    return;
+  }
+
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     tc::mbar_init(BAR(B_Q), 1);
@@ -158,6 +176,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const int half = c >> 3, cc = c & 7;
     auto slot_of = [&](int key) -> int {
       if (key >= w.kv_end) return -1;
+      if (p.ragged_kv) {  // contiguous K/V: key j of the request is row page_base + j
+        const long long row = (long long)ri.page_base + key;
+        if (row >= p.num_pages) {
+          record_error(err, PKV_DEVERR_PAGE_RANGE);
+          return -1;
+        }
+        return (int)row;
+      }
       const int lp = key / p.page_size;
       const int page = __ldg(p.kv_indices + ri.page_base + lp);
       if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages) {
@@ -286,7 +312,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const int g = r - (r / G) * G;
     const bool row_valid = t < w.q_rows;
     const int pos0 = ri.kv_len - ri.q_len + (w.q_row - ri.q_begin);  // position of the item's first token
-    const int P = pos0 + min(t, w.q_rows - 1);
+    // the row's last visible key: its own position (causal) or the request's last key
+    const int P = p.noncausal ? ri.kv_len - 1 : pos0 + min(t, w.q_rows - 1);
     const int lo = p.window_left >= 0 ? max(0, P - p.window_left) : 0;
     const uint32_t tS = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)x * 128;
     const uint32_t tO = tS + TMEM_O;

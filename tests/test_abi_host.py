@@ -235,3 +235,83 @@ def test_mixed_plan_with_only_decodes_needs_no_prefill_support(pk):
     with pytest.raises(pk.PkvError):  # an extend request with an FP8 cache is not supported
         pk.Plan().plan([0, 1, 3], [0, 2, 3], [3, 1, 0], [5, 16], num_qo_heads=32, num_kv_heads=8, head_dim=128,
                        page_size=16, mode="mixed", kv_dtype="e4m3", num_sms=152, host_only=True)
+
+
+# ---- ragged (contiguous K/V) and non-causal plans -------------------------------------------------
+def _extend(**kw):
+    a = dict(qo_indptr=[0, 40, 41, 300], kv_indptr=[0, 2, 3, 20], kv_indices=list(range(20)),
+             last_page_len=[10, 16, 16], num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+             mode="prefill", num_sms=152)
+    a.update(kw)
+    idx = [a.pop(k) for k in ("qo_indptr", "kv_indptr", "kv_indices", "last_page_len")]
+    return pk_plan_host(*idx, **a)
+
+
+def pk_plan_host(*idx, **a):
+    import paged_kv_attention_slot_gb300 as pk
+
+    return pk.Plan().plan(*idx, host_only=True, **a)
+
+
+@pytest.mark.parametrize("bad, status", [
+    (dict(causal=False, mode="decode", qo_indptr=[0, 1, 2, 3]), "PKV_EINVAL"),  # non-causal decode plan
+    (dict(causal=False, mode="mixed"), "PKV_EINVAL"),
+    (dict(causal=False, window_left=16), "PKV_EINVAL"),  # a window needs the causal mask
+    (dict(mode="ragged", kv_indptr=[0, 50, 40, 300]), "PKV_EINVAL"),  # ragged rows not non-decreasing
+    (dict(mode="ragged", kv_indptr=[0, 39, 40, 300]), "PKV_EINVAL"),  # causal: 39 keys for 40 queries
+    (dict(mode="ragged", kv_indptr=[1, 40, 41, 300]), "PKV_EINVAL"),
+])
+def test_plan_rejects_invalid_ragged_and_noncausal(pk, bad, status):
+    with pytest.raises(pk.PkvError) as ei:
+        _extend(**bad)
+    assert ei.value.args[0].startswith(status)
+
+
+def test_status_codes_of_causal_argument(pk):
+    import ctypes as C
+
+    a, keep = pk.Plan._args([0, 2], [0, 1], [0], [2], 8, 2, 128, 16, "prefill", -1, 0.0, "bf16", 0, 152)
+    a.causal = 2
+    n = C.c_size_t(0)
+    assert pk._lib.lib().pkv_plan_workspace_size(C.byref(a), C.byref(n)) == pk._lib.PKV_EINVAL
+
+
+def _prefill_items(p):
+    return [tuple(r) for r in p.work_items()[p.info()["num_decode_work"]:].tolist()]
+
+
+def test_ragged_plan_reads_each_requests_rows(pk):
+    # self-attention over fresh segments: kv rows = qo rows, causal, no page table at all
+    qo = [0, 5, 5, 300, 301]
+    p = pk.Plan().plan(qo, qo, None, None, num_qo_heads=8, num_kv_heads=2, head_dim=128, mode="ragged",
+                       num_sms=152, host_only=True)
+    info = p.info()
+    assert info["max_page_id"] == 300  # the largest K/V row read
+    assert info["num_prefill_tokens"] == 301
+    tok = 2 * 128 // 4  # tokens per CTA (two 128-row tiles of 4 heads per KV head)
+    for req, h, hg, k0, k1, q_row, slot, q_rows in _prefill_items(p):
+        n = qo[req + 1] - qo[req]
+        t0 = q_row - qo[req]
+        assert k0 == 0 and k1 == min(t0 + tok, n) and q_rows == min(tok, n - t0)  # causal: keys up to the last row
+
+
+def test_noncausal_plan_reads_the_whole_segment_and_allows_short_or_empty_ones(pk):
+    # the prefix pass of an extend: L_i prefix keys, n_i > L_i allowed, L_i = 0 gives an empty item
+    qo = [0, 100, 130, 200]
+    kv_len = [7, 0, 1000]
+    ps = 16
+    pages = [(L + ps - 1) // ps for L in kv_len]
+    indptr = np.concatenate([[0], np.cumsum(pages)]).tolist()
+    last = [L - (n - 1) * ps if n else 0 for L, n in zip(kv_len, pages)]
+    p = pk.Plan().plan(qo, indptr, list(range(indptr[-1])), last, num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                       page_size=ps, mode="prefill", causal=False, num_sms=152, host_only=True)
+    for req, h, hg, k0, k1, q_row, slot, q_rows in _prefill_items(p):
+        assert (k0, k1) == (0, kv_len[req])
+
+
+def test_merge_state_argument_checks(pk):
+    L = pk._lib.lib()
+    assert L.pkv_merge_state(None, None, None, None, None, None, 0, 128, None) == pk._lib.PKV_OK  # no states
+    assert L.pkv_merge_state(16, 16, 16, 16, 16, None, 4, 96, None) == pk._lib.PKV_EUNSUPPORTED
+    assert L.pkv_merge_state(16, 16, None, 16, 16, None, 4, 128, None) == pk._lib.PKV_EINVAL
+    assert L.pkv_merge_state(16, 16, 16, 16, 16, None, -1, 128, None) == pk._lib.PKV_EINVAL
