@@ -179,7 +179,8 @@ typedef struct pkv_plan_args {
   int32_t q_dtype;       /* PKV_BF16                                                         */
   int32_t kv_dtype;      /* PKV_BF16 or PKV_FP8_E4M3 (FP8 KV: decode mode only)               */
   int32_t max_splits;    /* split-KV chunks per (request, KV head): 0 = planner's choice,    */
-                         /* 1 = never split, k > 1 = at most k                               */
+                         /* 1 = never split, k > 1 = at most k.  Prefill items are split only */
+                         /* when there are fewer of them than SMs (at most 64 chunks each)    */
   int32_t num_sms;       /* SMs to plan for; 0 = query the current device                    */
 } pkv_plan_args;
 
@@ -321,13 +322,17 @@ typedef struct pkv_plan_info {
   int64_t num_decode_tokens;  /* their token rows                                            */
   int64_t num_prefills;       /* requests planned for the prefill kernel                     */
   int64_t num_prefill_tokens; /* their token rows                                            */
+  int64_t num_prefill_partials; /* prefill split-KV partial states (256 rows each)            */
 } pkv_plan_info;
 
 int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info);
 
 /* Copy the plan's work list to host memory: 8 int32 per CTA, in launch order:
  *   {request, kv_head, head_group, kv_begin, kv_end, q_row, out_slot, q_rows}
- * (out_slot = partial slot or -1 when the CTA writes the final output).  A decode CTA with
+ * (out_slot = partial slot or -1 when the CTA writes the final output; decode and prefill items
+ * number their partial slots separately).  A prefill item with a partial slot reads exactly
+ * [kv_begin, kv_end), a whole number of 128-key tiles except at the end of the item's range; the
+ * prefill run merges the pieces of each item with a second kernel.  A decode CTA with
  * out_slot = -1 reads all of [kv_begin, kv_end); the CTAs with consecutive partial slots of one
  * (request, kv_head, head_group) share the same [kv_begin, kv_end) and divide its 64-key groups
  * among themselves at run time (each warp starts on its own group, then takes the next unclaimed

@@ -34,7 +34,7 @@ from . import _lib
 from ._lib import PkvError, check, lib
 
 __all__ = [
-    "KVCache", "Plan", "PkvError", "kv_store", "merge_state", "device_error", "block_table_to_csr",
+    "KVCache", "Plan", "CascadePlan", "PkvError", "kv_store", "merge_state", "device_error", "block_table_to_csr",
     "token_table_to_page_table", "library_path",
 ]
 
@@ -260,6 +260,56 @@ class Plan:
             check(fn(self._h, q.data_ptr(), C.byref(cache.struct), out.data_ptr(),
                      lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
         return (out, lse) if (return_lse or lse is not None) else out
+
+
+class CascadePlan:
+    """Attention for a batch whose requests share a prefix, with the shared part computed once.
+
+    "vLLM 源码完全拆解（六）：Attention Backend", section «Cascade Attention 把共享前缀只算一次»: each
+    query's attention is split into the shared prefix and its request's own suffix, and the two
+    outputs are combined by their log-sum-exp weights.  Level 0 is one non-causal prefill plan in
+    which a single "request" holds every query row of the batch and the shared pages (so each
+    shared K/V tile is read once per query tile instead of once per request); level 1 is an ordinary
+    causal plan over each request's own suffix pages (decode when every request has one new token).
+    The run is three library calls: level 0 into ``out``/``lse``, level 1 into buffers kept by this
+    object, and pkv_merge_state in place.
+    """
+
+    def __init__(self):
+        self.shared = Plan()
+        self.suffix = Plan()
+        self._o2 = self._s2 = None
+
+    def plan(self, qo_indptr, shared_kv_indices, shared_last_page_len: int, kv_indptr, kv_indices, last_page_len, *,
+             num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale=0.0, num_sms=0, max_splits=0,
+             stream=None) -> "CascadePlan":
+        """shared_kv_indices: the shared prefix's pages in order (its last page holds
+        shared_last_page_len tokens); kv_indptr / kv_indices / last_page_len: each request's own
+        suffix pages (the suffix holds the new tokens, so every request with a new token has one)."""
+        qo = _i32(qo_indptr)
+        shared = _i32(shared_kv_indices)
+        kw = dict(num_qo_heads=num_qo_heads, num_kv_heads=num_kv_heads, head_dim=head_dim, page_size=page_size,
+                  sm_scale=sm_scale, num_sms=num_sms, max_splits=max_splits, stream=stream)
+        T = int(qo[-1]) if len(qo) else 0
+        self.shared.plan([0, T], [0, len(shared)], shared, [shared_last_page_len if len(shared) else 0],
+                         mode="prefill", causal=False, **kw)
+        n = np.diff(qo)
+        mode = "decode" if np.all(n <= 1) else ("mixed" if np.any(n == 1) else "prefill")
+        self.suffix.plan(qo, kv_indptr, kv_indices, last_page_len, mode=mode, **kw)
+        self.total_tokens = T
+        return self
+
+    def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+            return_lse: bool = False, stream=None):
+        if lse is None:
+            lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        out, lse = self.shared.run(q, cache, out=out, lse=lse, stream=stream)
+        if self._o2 is None or self._o2.shape != q.shape or self._o2.device != q.device:
+            self._o2 = torch.empty_like(q)
+            self._s2 = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+        self.suffix.run(q, cache, out=self._o2, lse=self._s2, stream=stream)
+        merge_state(out, lse, self._o2, self._s2, out=out, lse_out=lse, stream=stream)
+        return (out, lse) if return_lse else out
 
 
 def merge_state(o_a: torch.Tensor, lse_a: torch.Tensor, o_b: torch.Tensor, lse_b: torch.Tensor,

@@ -97,6 +97,7 @@ class pkv_plan_info(C.Structure):
         ("num_decode_tokens", C.c_int64),
         ("num_prefills", C.c_int64),
         ("num_prefill_tokens", C.c_int64),
+        ("num_prefill_partials", C.c_int64),
     ]
 
 

@@ -51,6 +51,9 @@ constexpr int kDecodeMinChunk = 256;     // never split below this many keys
 constexpr int kDecodeChunkAlign = 64;    // 4 warps x 16 keys
 constexpr int kPrefillRows = 128;        // query rows (tokens x heads of one KV head) per Q tile
 constexpr int kPrefillTiles = 2;         // Q tiles per CTA (they share every K/V tile)
+constexpr int kPrefillKeyTile = 128;     // keys per K/V tile of the prefill kernel
+constexpr int kPrefillMinChunk = 512;    // never split a prefill key range below this many keys
+constexpr int kPrefillMaxSplits = 64;    // chunks per prefill item at most (the chunk grows instead)
 
 }  // namespace
 
@@ -217,6 +220,8 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   P->kv_tokens = 0;
   P->kv_chunk = 0;
   P->num_decode_work = 0;
+  P->num_decode_merge = 0;
+  P->num_prefill_partials = 0;
   P->num_decodes = P->num_decode_tokens = P->num_prefills = P->num_prefill_tokens = 0;
 
   // decode rows: every request in decode mode, the one-token requests in mixed mode
@@ -328,6 +333,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     P->num_partials = slot;
   }
   P->num_decode_work = (int64_t)P->work.size();
+  P->num_decode_merge = (int64_t)P->merge.size();
   if (plan_prefill) {
     const int32_t tok_per_tile = kPrefillTiles * (kPrefillRows / G);  // tokens per CTA
     for (int32_t i = 0; i < B; ++i) {
@@ -360,6 +366,53 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
         }
       }
     }
+    // Split-KV for prefill items: when they cannot fill one wave (one CTA per SM) -- a few long
+    // requests, or a shared prefix attended by all of a batch's queries -- cut the long key ranges
+    // into chunks of whole key tiles.  Each piece writes a normalised fp32 partial state and its
+    // log2-sum-exp; a merge kernel combines the pieces of an item (the split-KV merge of
+    // "SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种形态», per row).
+    const size_t first = (size_t)P->num_decode_work;
+    const int64_t n_items = (int64_t)(P->work.size() - first);
+    if (a->max_splits != 1 && n_items > 0 && n_items < sms) {
+      int64_t total = 0;
+      for (size_t k = first; k < P->work.size(); ++k) total += P->work[k].kv_end - P->work[k].kv_begin;
+      int64_t chunk = std::max<int64_t>(align_up((total + sms - 1) / sms, kPrefillKeyTile), kPrefillMinChunk);
+      std::vector<WorkItem> items(P->work.begin() + first, P->work.end());
+      P->work.resize(first);
+      int64_t pslot = 0;
+      for (const WorkItem& it : items) {
+        const int64_t len = it.kv_end - it.kv_begin;
+        int64_t ns = len <= chunk + chunk / 4 ? 1 : (len + chunk - 1) / chunk;
+        ns = std::min<int64_t>(ns, a->max_splits > 1 ? std::min(a->max_splits, kPrefillMaxSplits) : kPrefillMaxSplits);
+        if (ns <= 1) {
+          P->work.push_back(it);
+          continue;
+        }
+        const int64_t piece = align_up((len + ns - 1) / ns, kPrefillKeyTile);
+        ns = (len + piece - 1) / piece;
+        MergeItem m{};
+        m.q_row = it.q_row;
+        m.kv_head = it.kv_head;
+        m.head_group = 0;
+        m.first_slot = (int32_t)pslot;
+        m.num_splits = (int32_t)ns;
+        m.q_rows = it.q_rows;
+        const int32_t unit = (int32_t)P->merge.size();
+        P->merge.push_back(m);
+        for (int64_t sp = 0; sp < ns; ++sp) {
+          WorkItem w = it;
+          w.kv_begin = (int32_t)(it.kv_begin + sp * piece);
+          w.kv_end = (int32_t)std::min<int64_t>(it.kv_end, it.kv_begin + (sp + 1) * piece);
+          w.out_slot = (int32_t)(pslot + sp);
+          w.split = (int32_t)sp;
+          w.num_splits = (int32_t)ns;
+          w.unit = unit;
+          P->work.push_back(w);
+        }
+        pslot += ns;
+      }
+      P->num_prefill_partials = pslot;
+    }
   }
   // longest first: the block scheduler hands out CTAs roughly in launch order
   order_longest_first(P->work, 0, (size_t)P->num_decode_work);
@@ -385,6 +438,10 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   off = align_up(off + (size_t)P->num_partials * pkv::kDecodeRows * sizeof(float), 256);
   P->off_po = off;
   off = align_up(off + (size_t)P->num_partials * pkv::kDecodeRows * P->D * sizeof(float), 256);
+  P->off_pplse = off;
+  off = align_up(off + (size_t)P->num_prefill_partials * pkv::kPrefillItemRows * sizeof(float), 256);
+  P->off_ppo = off;
+  off = align_up(off + (size_t)P->num_prefill_partials * pkv::kPrefillPartialFloats * sizeof(float), 256);
   P->need_bytes = std::max<size_t>(off, 256);
   P->valid = true;
   return PKV_OK;
@@ -423,6 +480,8 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
   p.kv_indices = (const int32_t*)(ws + P->off_idx);
   p.part_lse = (float*)(ws + P->off_plse);
   p.part_o = (float*)(ws + P->off_po);
+  p.ppart_lse = (float*)(ws + P->off_pplse);
+  p.ppart_o = (float*)(ws + P->off_ppo);
   p.unit_count = (int32_t*)(ws + P->off_count);
   p.claim = (int32_t*)(ws + P->off_claim);
   p.q = q;
@@ -666,6 +725,9 @@ int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* 
   }
   pkv::RunParams p = make_params(plan, q, cache, o, lse, first, count);
   PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
+  const int64_t nm = (int64_t)plan->merge.size() - plan->num_decode_merge;
+  if (nm > 0)
+    PKV_CUDA(pkv::launch_prefill_merge(p, plan->num_decode_merge, nm, (cudaStream_t)stream), "prefill merge launch");
   return PKV_OK;
 }
 }  // namespace
@@ -736,6 +798,7 @@ int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info) {
   info->num_decode_tokens = plan->num_decode_tokens;
   info->num_prefills = plan->num_prefills;
   info->num_prefill_tokens = plan->num_prefill_tokens;
+  info->num_prefill_partials = plan->num_prefill_partials;
   return PKV_OK;
 }
 

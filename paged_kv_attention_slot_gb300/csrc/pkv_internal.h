@@ -28,14 +28,16 @@ struct WorkItem {
 static_assert(sizeof(WorkItem) == 48, "WorkItem is 48 bytes");
 constexpr int kWorkItemPublicFields = 8;
 
-// One (request, KV head, head group) whose split-KV partials must be merged.
+// One (request, KV head, head group) whose split-KV partials must be merged.  Decode units come
+// first in the plan's list; a prefill unit (a two-tile query item cut into key chunks) follows them.
 struct MergeItem {
   int32_t q_row;
   int32_t kv_head;
   int32_t head_group;
   int32_t first_slot;
   int32_t num_splits;
-  int32_t pad0, pad1, pad2;
+  int32_t q_rows;  // prefill: tokens of the item (decode: 1)
+  int32_t pad1, pad2;
 };
 static_assert(sizeof(MergeItem) == 32, "MergeItem is 32 bytes");
 
@@ -55,6 +57,11 @@ constexpr int kClaimStride = 32;
 // Max query rows one decode CTA handles per KV head (one m16 MMA tile).
 constexpr int kDecodeRows = 16;
 
+// Query rows of one prefill CTA (two 128-row tiles) and the layout of one prefill partial slot:
+// lse [256] (log2 units), then O as [32 four-column groups][256 rows] float4 (coalesced per group).
+constexpr int kPrefillItemRows = 256;
+constexpr int kPrefillPartialFloats = kPrefillItemRows * 128;
+
 // Everything a run kernel reads, passed by value.
 struct RunParams {
   const WorkItem* work;
@@ -63,6 +70,8 @@ struct RunParams {
   const int32_t* kv_indices;
   float* part_o;    // [num_partials, 16, head_dim]
   float* part_lse;  // [num_partials, 16] (log2 units)
+  float* ppart_o;    // prefill: [prefill partials, 32, 256, 4] normalised fp32 O
+  float* ppart_lse;  // prefill: [prefill partials, 256] log2-sum-exp (-inf = no visible key)
   int32_t* unit_count;       // [num_merge]: partials written so far (0 between runs)
   int32_t* claim;            // [num_merge * kClaimStride]: groups claimed beyond the static ones (0 between runs)
   const void* q;
@@ -96,6 +105,7 @@ int decode_ctas_per_sm(int kv_dtype, int head_dim, int group);  // resident deco
 cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v,
                            int64_t total_tokens, cudaStream_t s);
 int prefill_supported(const char** why);
+cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s);
 cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o,
                                float* lse, int64_t num_states, int head_dim, cudaStream_t s);
 
@@ -115,12 +125,15 @@ struct pkv_plan {
   float sm_scale = 0.f;
   int64_t total_tokens = 0, max_page_id = -1, kv_tokens = 0, kv_chunk = 0, num_partials = 0;
   int64_t num_decode_work = 0;  // the decode kernel's items come first in `work`, the prefill kernel's after
+  int64_t num_decode_merge = 0;  // decode merge units first in `merge`, prefill units after
+  int64_t num_prefill_partials = 0;
   int64_t num_decodes = 0, num_decode_tokens = 0, num_prefills = 0, num_prefill_tokens = 0;
   std::vector<pkv::WorkItem> work;
   std::vector<pkv::MergeItem> merge;
   std::vector<pkv::ReqInfo> req;
   std::vector<int32_t> indices;
   size_t off_work = 0, off_merge = 0, off_req = 0, off_idx = 0, off_count = 0, off_claim = 0, off_plse = 0, off_po = 0;
+  size_t off_pplse = 0, off_ppo = 0;  // prefill partials
   size_t meta_bytes = 0, need_bytes = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;

@@ -378,7 +378,28 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       if (lane == 0) tc::mbar_arrive(BAR(B_PF + x));
     }
     if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD + x), 0, abort_flag, WAIT_LIMIT));
-    if (ok) {
+    if (ok && w.out_slot >= 0) {
+      // one key chunk of a split item: normalised fp32 partial + log2-sum-exp, merged afterwards.
+      // O goes out as [32 four-column groups][256 rows] float4, so each store is coalesced.
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int prow = x * ROWS + r;
+      float4* dst = reinterpret_cast<float4*>(p.ppart_o + (int64_t)w.out_slot * kPrefillPartialFloats) + prow;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t o[32];
+        tc::tmem_ld32(tO + h * 32, o);
+        if (row_valid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[(h * 8 + q) * kPrefillItemRows] =
+                make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                            __uint_as_float(o[4 * q + 2]) * inv, __uint_as_float(o[4 * q + 3]) * inv);
+        }
+      }
+      if (row_valid)
+        p.ppart_lse[(int64_t)w.out_slot * kPrefillItemRows + prow] = l > 0.f ? m_used + __log2f(l) : -INFINITY;
+    } else if (ok) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const int head = w.kv_head * G + g;
@@ -415,6 +436,63 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }
 #undef BAR
+}
+
+// Merge of the key chunks of split prefill items: one CTA per item, thread r = row r of the item's
+// two tiles (the same (token, head) order as the prefill kernel).  m = max_s lse_s, w_s =
+// 2^(lse_s - m) / sum_s 2^(lse_s - m), o = sum_s w_s o_s; rows whose chunks saw no key get o = 0 and
+// lse = -inf.
+__global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const RunParams p, int64_t first_merge) {
+  const MergeItem m = p.merge[first_merge + blockIdx.x];
+  const int r = threadIdx.x;
+  const int G = p.group;
+  const int T = pf::ROWS / G;
+  const int x = r / pf::ROWS, rr = r % pf::ROWS;
+  const int t = x * T + rr / G, g = rr % G;
+  if (t >= m.q_rows) return;
+  const float* lse_s = p.ppart_lse + (int64_t)m.first_slot * kPrefillItemRows + r;
+  float mx = -INFINITY;
+  for (int sp = 0; sp < m.num_splits; ++sp) mx = fmaxf(mx, lse_s[(int64_t)sp * kPrefillItemRows]);
+  float4 acc[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float sum = 0.f;
+  if (mx != -INFINITY) {
+    for (int sp = 0; sp < m.num_splits; ++sp) {
+      const float wgt = ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
+      sum += wgt;
+      if (wgt == 0.f) continue;
+      const float4* src =
+          reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) * kPrefillPartialFloats) + r;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float4 v = src[c * kPrefillItemRows];
+        acc[c].x = fmaf(wgt, v.x, acc[c].x);
+        acc[c].y = fmaf(wgt, v.y, acc[c].y);
+        acc[c].z = fmaf(wgt, v.z, acc[c].z);
+        acc[c].w = fmaf(wgt, v.w, acc[c].w);
+      }
+    }
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  const int64_t row = (int64_t)(m.q_row + t);
+  const int head = m.kv_head * G + g;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    uint4 u;
+    u.x = pack_bf16(acc[2 * c].x * inv, acc[2 * c].y * inv);
+    u.y = pack_bf16(acc[2 * c].z * inv, acc[2 * c].w * inv);
+    u.z = pack_bf16(acc[2 * c + 1].x * inv, acc[2 * c + 1].y * inv);
+    u.w = pack_bf16(acc[2 * c + 1].z * inv, acc[2 * c + 1].w * inv);
+    dst[c] = u;
+  }
+  if (p.lse) p.lse[row * p.num_qo_heads + head] = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
+}
+
+cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s) {
+  prefill_merge_kernel<<<(unsigned)count, kPrefillItemRows, 0, s>>>(p, first_merge);
+  return cudaGetLastError();
 }
 
 int prefill_supported(const char** why) {

@@ -304,9 +304,19 @@ def test_noncausal_plan_reads_the_whole_segment_and_allows_short_or_empty_ones(p
     indptr = np.concatenate([[0], np.cumsum(pages)]).tolist()
     last = [L - (n - 1) * ps if n else 0 for L, n in zip(kv_len, pages)]
     p = pk.Plan().plan(qo, indptr, list(range(indptr[-1])), last, num_qo_heads=8, num_kv_heads=2, head_dim=128,
-                       page_size=ps, mode="prefill", causal=False, num_sms=152, host_only=True)
+                       page_size=ps, mode="prefill", causal=False, num_sms=152, max_splits=1, host_only=True)
     for req, h, hg, k0, k1, q_row, slot, q_rows in _prefill_items(p):
         assert (k0, k1) == (0, kv_len[req])
+    # with splitting allowed, the pieces of each (request, head, query tile) still cover [0, L) once
+    p = pk.Plan().plan(qo, indptr, list(range(indptr[-1])), last, num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                       page_size=ps, mode="prefill", causal=False, num_sms=152, host_only=True)
+    cover = {}
+    for req, h, hg, k0, k1, q_row, slot, q_rows in _prefill_items(p):
+        cover.setdefault((req, h, q_row), []).append((k0, k1))
+    for (req, h, q_row), pieces in cover.items():
+        pieces.sort()
+        assert pieces[0][0] == 0 and pieces[-1][1] == kv_len[req]
+        assert all(a[1] == b_[0] for a, b_ in zip(pieces, pieces[1:]))
 
 
 def test_merge_state_argument_checks(pk):
@@ -315,3 +325,54 @@ def test_merge_state_argument_checks(pk):
     assert L.pkv_merge_state(16, 16, 16, 16, 16, None, 4, 96, None) == pk._lib.PKV_EUNSUPPORTED
     assert L.pkv_merge_state(16, 16, None, 16, 16, None, 4, 128, None) == pk._lib.PKV_EINVAL
     assert L.pkv_merge_state(16, 16, 16, 16, 16, None, -1, 128, None) == pk._lib.PKV_EINVAL
+
+
+# ---- prefill split-KV --------------------------------------------------------------------------------
+def _prefill_pieces(p):
+    info = p.info()
+    return p.work_items()[info["num_decode_work"]:], info
+
+
+@pytest.mark.parametrize("causal, window", [(True, -1), (False, -1), (True, 3000)])
+def test_prefill_split_covers_every_key_once(pk, causal, window):
+    # few items (one request, 2 KV heads, 64 tokens): long key ranges are cut into 128-key-tile chunks
+    L, n, ps = 20000, 64, 16
+    npg = (L + ps - 1) // ps
+    p = pk.Plan().plan([0, n], [0, npg], list(range(npg)), [L - (npg - 1) * ps], num_qo_heads=8, num_kv_heads=2,
+                       head_dim=128, page_size=ps, mode="prefill", causal=causal, window_left=window,
+                       num_sms=152, host_only=True)
+    items, info = _prefill_pieces(p)
+    assert info["num_prefill_partials"] == len(items) > 2
+    by_head = {}
+    for req, h, hg, k0, k1, q_row, slot, q_rows in items.tolist():
+        assert slot >= 0 and q_rows == n and q_row == 0
+        by_head.setdefault(h, []).append((k0, k1, slot))
+    lo = 0 if window < 0 else max(0, L - n - window)
+    hi = L if not causal else L  # causal: the last row is at position L - 1
+    slots = []
+    for h, pieces in by_head.items():
+        pieces.sort()
+        assert pieces[0][0] == lo and pieces[-1][1] == hi
+        for (a0, a1, _), (b0, b1, _) in zip(pieces, pieces[1:]):
+            assert a1 == b0 and (a1 - a0) % 128 == 0
+        slots += [s_ for _, _, s_ in pieces]
+    assert sorted(slots) == list(range(len(slots)))
+    assert info["num_merge"] == 2
+
+
+def test_prefill_split_respects_max_splits_and_many_items(pk):
+    L, n, ps = 20000, 64, 16
+    npg = (L + ps - 1) // ps
+    args = ([0, n], [0, npg], list(range(npg)), [L - (npg - 1) * ps])
+    kw = dict(num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=ps, mode="prefill", host_only=True)
+    never = pk.Plan().plan(*args, max_splits=1, num_sms=152, **kw)
+    assert never.info()["num_prefill_partials"] == 0 and never.info()["num_work"] == 2
+    three = pk.Plan().plan(*args, max_splits=3, num_sms=152, **kw)
+    assert three.info()["num_work"] == 6 and three.info()["num_prefill_partials"] == 6
+    # the prefix-extend workload fills many waves on its own: no split
+    import workloads as W
+
+    b = W.workload(3)
+    big = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
+                         head_dim=128, page_size=1, mode="prefill", num_sms=152, host_only=True)
+    assert big.info()["num_prefill_partials"] == 0 and big.info()["num_merge"] == 0

@@ -218,3 +218,21 @@ def test_extend_by_merge_full_size_prefix_extend_sampled():
     ro, rl = G.oracle_attention(b, kp, vp, fmt, rows=rows)
     G.compare(out, lse, ro, rl, rows=rows)
     assert rag.info()["num_work"] > 500 and pre.info()["num_work"] > 500
+
+
+def test_split_noncausal_prefix_and_ragged_segments():
+    # a long cached prefix attended by few queries (split), merged with the new tokens' ragged pass
+    b = W.make_batch([9000, 40], [48, 40], 16, 32, 8, 128, seed=90)
+    g = G.GpuBatch(b)
+    g.store()
+    out, lse, (rag, pre) = extend_by_merge(b, g)
+    assert pre.info()["num_prefill_partials"] > 0
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt)
+    G.compare(out, lse, ro, rl)
+
+
+def test_split_ragged_long_kv():
+    # contiguous K/V much longer than the queries: a split ragged pass
+    out, lse, ro, rl = _ragged_case([12000, 64], [32, 64], 16, 4, seed=91)
+    _compare_with_empty(out, lse, ro, rl)

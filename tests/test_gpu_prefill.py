@@ -79,3 +79,28 @@ def test_prefill_full_size_prefix_extend_sampled():
         rows += [q0, q1 - 1] + rng.integers(q0, q1, size=3).tolist()
     stats, plan = _case(b, rows=sorted(set(rows)))
     assert plan.info()["num_work"] > 1000
+
+
+# ---- split-KV prefill: few query items over long key ranges --------------------------------------
+def test_prefill_split_long_prefix_few_tokens():
+    # one request, 64 new tokens after a 20k-token prefix: 8 items on 152 SMs, so the planner cuts
+    # each key range into chunks and a merge kernel combines them
+    b = W.make_batch([20000], [64], 16, 32, 8, 128, seed=80)
+    stats, plan = _case(b)
+    info = plan.info()
+    assert info["num_prefill_partials"] > 8 and info["num_merge"] == 8
+
+
+@pytest.mark.parametrize("window", [-1, 700])
+def test_prefill_split_forced_on_many_items(window):
+    # a large planning SM count forces splits on a batch with ragged tiles, GQA 4 and page size 1
+    b = W.make_batch([3000, 200, 2500], [300, 200, 1], 1, 16, 4, 128, seed=81, window_left=window)
+    stats, plan = _case(b, num_sms=4096)
+    assert plan.info()["num_prefill_partials"] > 0
+
+
+def test_prefill_split_respects_max_splits():
+    b = W.make_batch([5000, 1500], [100, 64], 16, 8, 2, 128, seed=82)
+    stats, plan = _case(b, num_sms=4096, max_splits=3)
+    items = plan.work_items()
+    assert items[:, 6].max() >= 0 and plan.info()["num_prefill_partials"] <= 3 * plan.info()["num_merge"]

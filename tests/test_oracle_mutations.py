@@ -25,6 +25,7 @@ CHECKS = [
     ("ragged_bruteforce", P.check_ragged_bruteforce),
     ("ragged_bruteforce_noncausal", lambda: P.check_ragged_bruteforce(causal=False)),
     ("ragged_sdpa", P.check_ragged_sdpa),
+    ("cascade", P.check_cascade_shared_prefix),
 ]
 
 

@@ -453,6 +453,48 @@ def test_noncausal_paged_segment_without_keys_is_the_empty_state():
     assert np.all(np.isfinite(lse[: b["qo_indptr"][1]]))
 
 
+def check_cascade_shared_prefix(seed=14):
+    """"vLLM 源码完全拆解（六）：Attention Backend", section «Cascade Attention 把共享前缀只算一次»: when the
+    requests of a batch share a prefix, each query's attention splits into the shared prefix (computed
+    once for all queries: one "request" holding every query row, all prefix keys visible) and its own
+    suffix (causal), merged by their LSE weights -- equal to each request's flat causal pass."""
+    rng = np.random.default_rng(seed)
+    ps, Hq, Hkv, D = 4, 4, 2, 8
+    shared_pages = 3
+    suffix = [5, 1, 9, 4]
+    n = [1, 1, 3, 4]
+    Lp = shared_pages * ps
+    own = [(x + ps - 1) // ps for x in suffix]
+    P = shared_pages + sum(own) + 2
+    kp, vp = rng.normal(size=(P, ps, Hkv, D)), rng.normal(size=(P, ps, Hkv, D))
+    perm = rng.permutation(P)
+    shared = perm[:shared_pages]
+    rows, at = [], shared_pages
+    for c in own:
+        rows.append(perm[at:at + c])
+        at += c
+    q = rng.normal(size=(sum(n), Hq, D)) * 2
+    qo = np.concatenate([[0], np.cumsum(n)])
+    last = [x - (c - 1) * ps for x, c in zip(suffix, own)]
+    # flat: every request's page list = shared pages + its own pages
+    flat_ptr = np.concatenate([[0], np.cumsum([shared_pages + c for c in own])])
+    flat_idx = np.concatenate([np.concatenate([shared, r]) for r in rows])
+    fo, fs = A.paged_attention(q, kp, vp, qo, flat_ptr, flat_idx, last, ps, sm_scale=0.35)
+    # level 0: all query rows as one request over the shared pages, non-causal
+    so, ss = A.paged_attention(q, kp, vp, [0, qo[-1]], [0, shared_pages], shared, [ps], ps, sm_scale=0.35,
+                               causal=False)
+    # level 1: each request over its own suffix pages, causal
+    uo, us = A.paged_attention(q, kp, vp, qo, np.concatenate([[0], np.cumsum(own)]), np.concatenate(rows), last, ps,
+                               sm_scale=0.35)
+    mo, ms = A.merge_states(so, ss, uo, us)
+    assert Lp == 12
+    return bool(np.allclose(mo, fo, rtol=0, atol=1e-13) and np.allclose(ms, fs, rtol=0, atol=1e-12))
+
+
+def test_cascade_shared_prefix_merge_equals_flat_causal():
+    assert check_cascade_shared_prefix()
+
+
 def test_bruteforce_tiny():
     assert check_bruteforce()
 

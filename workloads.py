@@ -109,22 +109,33 @@ def make_batch(
     sm_scale: float = 0.0,
     name: str = "custom",
     mode: str | None = None,
+    shared_prefix: int = 0,
 ) -> Batch:
-    """Build one seeded batch.  kv_lens[i] >= q_lens[i] >= 0; a request with kv_len 0 owns no page."""
+    """Build one seeded batch.  kv_lens[i] >= q_lens[i] >= 0; a request with kv_len 0 owns no page.
+
+    ``shared_prefix`` > 0 (a multiple of page_size): the first shared_prefix tokens of every request
+    live on the SAME physical pages (a common system prompt); each request's remaining kv_len -
+    shared_prefix tokens, which hold its q_len new tokens, are on pages of its own.
+    """
     kv_len = np.asarray(kv_lens, dtype=np.int64)
     q_len = np.asarray(q_lens, dtype=np.int64)
     if kv_len.shape != q_len.shape or np.any(q_len < 0) or np.any(kv_len < q_len):
         raise ValueError("need kv_len >= q_len >= 0 per request")
+    if shared_prefix % page_size or np.any(kv_len - shared_prefix < q_len):
+        raise ValueError("the shared prefix must be whole pages and precede every request's new tokens")
     g = torch.Generator(device="cpu").manual_seed(int(seed))
-    counts = [(int(L) + page_size - 1) // page_size for L in kv_len]
-    need = sum(counts)
+    n_shared = shared_prefix // page_size
+    own = [(int(L) - shared_prefix + page_size - 1) // page_size for L in kv_len]
+    counts = [n_shared + c for c in own]
+    need = n_shared + sum(own)
     P = int(num_pages) if num_pages is not None else max(1, math.ceil(pool_factor * need))
     if P < need:
         raise ValueError(f"pool of {P} pages cannot hold {need}")
     perm = torch.randperm(P, generator=g).numpy().astype(np.int64)
-    rows, at = [], 0
-    for c in counts:
-        rows.append(perm[at : at + c].copy())
+    shared_rows = perm[:n_shared].copy()
+    rows, at = [], n_shared
+    for c in own:
+        rows.append(np.concatenate([shared_rows, perm[at : at + c]]))
         at += c
     k_pool = _randn_bf16(g, (P, page_size, num_kv_heads, head_dim))
     v_pool = _randn_bf16(g, (P, page_size, num_kv_heads, head_dim))
@@ -160,6 +171,7 @@ def make_batch(
         slot_mapping=np.asarray(slots, dtype=np.int64), q=q, k_new=k_new, v_new=v_new,
         k_pool=k_pool, v_pool=v_pool, kv_dtype=kv_dtype, k_scale=k_scale, v_scale=v_scale,
         window_left=window_left, sm_scale=sm_scale,
+        meta={"shared_prefix": int(shared_prefix), "shared_pages": shared_rows} if shared_prefix else {},
     )
 
 
@@ -173,6 +185,22 @@ WORKLOADS = {
     4: "Llama-3-70B-shaped ragged decode: batch 256, 64q/8kv, D 128, KV length log-normal median 1024, page 64",
     5: "long-context FP8-KV decode: batch 2, KV length 131072, 32q/8kv, D 128, e4m3 K/V, page 128",
 }
+
+
+def shared_prefix_workload(seed_offset: int = 0, batch: int = 64, shared_prefix: int = 4096,
+                           suffix_max: int = 512) -> Batch:
+    """Decode batch whose requests share a system prompt (the case cascade attention serves).
+
+    Llama-3-8B-shaped heads (32 q / 8 kv, head_dim 128), page size 16, a shared prefix of
+    ``shared_prefix`` tokens on common pages, and per-request suffixes of U[1, suffix_max] tokens
+    (the last of which is the new token), bf16 N(0, 1) values, seed 1006 (+ 100000 * seed_offset).
+    """
+    seed = 1006 + 100000 * int(seed_offset)
+    g = torch.Generator(device="cpu").manual_seed(seed + 7919)
+    suf = torch.randint(1, suffix_max + 1, (batch,), generator=g).tolist()
+    L = [shared_prefix + x for x in suf]
+    return make_batch(L, [1] * batch, 16, 32, 8, 128, seed, name="shared_prefix_decode", mode="decode",
+                      shared_prefix=shared_prefix)
 
 
 def workload(n: int, window_left: int = -1, scale_batch: float = 1.0, seed_offset: int = 0) -> Batch:
