@@ -481,6 +481,108 @@ def prefill_measure(device, steps, warmup, peak_tflops):
     }
 
 
+def _visible_pairs(kv_len, q_len):
+    import numpy as np
+
+    n = q_len.astype(np.float64)
+    p = (kv_len - q_len).astype(np.float64)
+    return float(np.sum(n * p + n * (n + 1) / 2))
+
+
+def next_rows_measure(device, peak_tflops, hbm):
+    """The widened paths, each timed as a replayed CUDA graph of its launches on resident inputs."""
+    import numpy as np
+    import torch
+
+    import paged_kv_attention_slot_gb300 as pk
+    import workloads as W
+
+    out = {}
+    # (1) prefix-cached extend in the paged + merge form: ragged pass over the new tokens' own K/V,
+    #     paged pass over the cached prefix (every prefix key visible), LSE merge in place
+    b = W.workload(3)
+    st = _device_state(b, device)
+    pk.kv_store(st["k_new"], st["v_new"], st["slots"], st["cache"])
+    kw = dict(num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, sm_scale=b.sm_scale)
+    rag = pk.Plan().plan(b.qo_indptr, b.qo_indptr, None, None, mode="ragged", **kw)
+    ps = b.page_size
+    pre_len = (b.kv_len - b.q_len).astype(np.int64)
+    npg = (pre_len + ps - 1) // ps
+    pi = np.concatenate([[0], np.cumsum(npg)]).astype(np.int32)
+    px = np.concatenate([b.kv_indices[b.kv_indptr[i]:b.kv_indptr[i] + npg[i]] for i in range(b.batch_size)])
+    pl = np.where(npg > 0, pre_len - (npg - 1) * ps, 0).astype(np.int32)
+    pre = pk.Plan().plan(b.qo_indptr, pi, px.astype(np.int32), pl, page_size=ps, mode="prefill", causal=False, **kw)
+    o1, s1 = torch.empty_like(st["q"]), torch.empty(st["q"].shape[:2], dtype=torch.float32, device=device)
+    o2, s2 = torch.empty_like(o1), torch.empty_like(s1)
+
+    def extend_by_merge():
+        rag.run_ragged(st["q"], st["k_new"], st["v_new"], out=o1, lse=s1)
+        pre.run(st["q"], st["cache"], out=o2, lse=s2)
+        pk.merge_state(o1, s1, o2, s2, out=o1, lse_out=s1)
+
+    flops = 4.0 * b.head_dim * b.num_qo_heads * _visible_pairs(b.kv_len, b.q_len)
+    ms, mode = kernel_ms(extend_by_merge, reps=10, iters=5)
+    out["extend_by_merge"] = {
+        "workload": "prefix_extend (as the prefill line) computed as ragged + paged prefix + merge",
+        "launches": 3 + (1 if pre.info()["num_merge"] else 0),
+        "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "frac": round(flops / (ms * 1e-3) / 1e12 / peak_tflops, 4), "timing": mode,
+        "plans": {"ragged_ctas": rag.info()["num_work"], "prefix_ctas": pre.info()["num_work"]}}
+    del st, rag, pre, o1, o2, s1, s2
+    torch.cuda.empty_cache()
+
+    # (2) cascade: batch-64 decode sharing a 4096-token system prompt, against the flat decode plan
+    b = W.shared_prefix_workload()
+    st = _device_state(b, device)
+    pk.kv_store(st["k_new"], st["v_new"], st["slots"], st["cache"])
+    flat = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **_plan_kw(b))
+    ns = len(b.meta["shared_pages"])
+    rows = [r[ns:] for r in b.block_rows]
+    suf = (b.kv_len - b.meta["shared_prefix"]).astype(np.int64)
+    si = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    sx = np.concatenate(rows).astype(np.int32)
+    sl = np.array([x - (len(r) - 1) * b.page_size for x, r in zip(suf, rows)], dtype=np.int32)
+    cas = pk.CascadePlan().plan(b.qo_indptr, b.meta["shared_pages"], b.page_size, si, sx, sl,
+                                num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
+                                page_size=b.page_size)
+    lse = torch.empty(st["q"].shape[:2], dtype=torch.float32, device=device)
+    flat_ms, mode = kernel_ms(lambda: flat.run(st["q"], st["cache"], out=st["out"]))
+    cas_ms, _ = kernel_ms(lambda: cas.run(st["q"], st["cache"], out=st["out"], lse=lse))
+    row_bytes = b.num_kv_heads * b.head_dim * 2 * 2
+    flat_bytes = int(b.kv_len.sum()) * row_bytes
+    unique_bytes = (b.meta["shared_prefix"] + int(suf.sum())) * row_bytes
+    out["cascade_decode"] = {
+        "workload": "shared_prefix_decode: batch 64, 32q/8kv, D 128, page 16, shared prefix 4096 + own suffix U[1,512]",
+        "flat_decode_ms": round(flat_ms, 4), "cascade_ms": round(cas_ms, 4),
+        "speedup": round(flat_ms / cas_ms, 3),
+        "flat_kv_bytes": flat_bytes, "unique_kv_bytes": unique_bytes,
+        "flat_gbs": round(flat_bytes / (flat_ms * 1e-3) / 1e9, 1),
+        "cascade_unique_gbs": round(unique_bytes / (cas_ms * 1e-3) / 1e9, 1),
+        "cascade_equivalent_gbs": round(flat_bytes / (cas_ms * 1e-3) / 1e9, 1),
+        "launches": 4, "timing": mode,
+        "plans": {"shared_ctas": cas.shared.info()["num_work"], "suffix_ctas": cas.suffix.info()["num_work"]}}
+    del st, flat, cas, lse
+    torch.cuda.empty_cache()
+
+    # (3) long prefix, short extend: 2 requests x 256 new tokens after a 32768-token prefix (64 items
+    #     on 152 SMs), with and without prefill split-KV
+    b = W.make_batch([32768 + 256] * 2, [256] * 2, 16, 32, 8, 128, seed=1107, name="long_prefix_extend")
+    st = _device_state(b, device)
+    pk.kv_store(st["k_new"], st["v_new"], st["slots"], st["cache"])
+    flops = 4.0 * b.head_dim * b.num_qo_heads * _visible_pairs(b.kv_len, b.q_len)
+    res = {"workload": "long_prefix_extend: batch 2, prefix 32768, 256 new tokens, page 16, 32q/8kv, D 128"}
+    for key, ms_ in (("split", 0), ("no_split", 1)):
+        pl_ = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, max_splits=ms_, **_plan_kw(b))
+        t, mode = kernel_ms(lambda: pl_.run(st["q"], st["cache"], out=st["out"]), reps=10, iters=5)
+        res[key] = {"ms": round(t, 4), "tflops": round(flops / (t * 1e-3) / 1e12, 2),
+                    "ctas": pl_.info()["num_work"], "partials": pl_.info()["num_prefill_partials"]}
+    res["timing"] = mode
+    out["long_prefix_extend"] = res
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -491,6 +593,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--only-prefill", action="store_true", help="measure the prefill workload alone (profiling)")
     ap.add_argument("--no-other-decode", action="store_true", help="skip the other decode workloads")
+    ap.add_argument("--no-next", action="store_true", help="skip the extend-by-merge / cascade / split measurements")
+    ap.add_argument("--only-next", action="store_true", help="measure those alone")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -500,6 +604,18 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, world, rank)
+    if args.only_next:
+        import torch
+
+        import paged_kv_attention_slot_gb300 as pk
+
+        torch.cuda.set_device(local_rank)
+        pk._lib.lib()
+        hbm, tf_burst, _, _ = _peaks()
+        res = next_rows_measure(torch.device("cuda", local_rank), tf_burst, hbm)
+        res["device_error"] = pk.device_error()
+        print(json.dumps(res))
+        return
     if args.only_prefill:
         import torch
 
@@ -559,6 +675,9 @@ def main():
     other = None
     if not args.no_other_decode and rank == 0:
         other = decode_other_configs(device, hbm)
+    nxt = None
+    if not args.no_next and rank == 0:
+        nxt = next_rows_measure(device, tf_burst, hbm)
 
     cpu = None
     if pool is not None:
@@ -600,6 +719,7 @@ def main():
             "cpu_baseline": cpu,
             "prefill": prefill,
             "decode_other_configs": other,
+            "next_rows": nxt,
             "device_error": pk.device_error() if err == 0 else err,
         }
         print(json.dumps(line))

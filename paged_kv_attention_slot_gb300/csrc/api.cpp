@@ -52,7 +52,7 @@ constexpr int kDecodeChunkAlign = 64;    // 4 warps x 16 keys
 constexpr int kPrefillRows = 128;        // query rows (tokens x heads of one KV head) per Q tile
 constexpr int kPrefillTiles = 2;         // Q tiles per CTA (they share every K/V tile)
 constexpr int kPrefillKeyTile = 128;     // keys per K/V tile of the prefill kernel
-constexpr int kPrefillMinChunk = 512;    // never split a prefill key range below this many keys
+constexpr int kPrefillMinChunk = 256;    // never split a prefill key range below this many keys
 constexpr int kPrefillMaxSplits = 64;    // chunks per prefill item at most (the chunk grows instead)
 
 }  // namespace
@@ -376,14 +376,27 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     if (a->max_splits != 1 && n_items > 0 && n_items < sms) {
       int64_t total = 0;
       for (size_t k = first; k < P->work.size(); ++k) total += P->work[k].kv_end - P->work[k].kv_begin;
+      const int64_t cap = a->max_splits > 1 ? std::min(a->max_splits, kPrefillMaxSplits) : kPrefillMaxSplits;
+      auto splits_of = [&](int64_t len, int64_t c) -> int64_t {
+        const int64_t ns = len <= c + c / 4 ? 1 : (len + c - 1) / c;
+        return std::min(ns, cap);
+      };
+      // smallest chunk (whole key tiles, at least kPrefillMinChunk) whose pieces fit one wave: the
+      // pieces of equally long items finish together, and a second, mostly idle wave costs as much
+      // as the first
       int64_t chunk = std::max<int64_t>(align_up((total + sms - 1) / sms, kPrefillKeyTile), kPrefillMinChunk);
+      auto pieces = [&](int64_t c) -> int64_t {
+        int64_t n = 0;
+        for (size_t k = first; k < P->work.size(); ++k) n += splits_of(P->work[k].kv_end - P->work[k].kv_begin, c);
+        return n;
+      };
+      for (int it = 0; it < 64 && pieces(chunk) > sms; ++it) chunk = align_up(chunk + chunk / 16, kPrefillKeyTile);
       std::vector<WorkItem> items(P->work.begin() + first, P->work.end());
       P->work.resize(first);
       int64_t pslot = 0;
       for (const WorkItem& it : items) {
         const int64_t len = it.kv_end - it.kv_begin;
-        int64_t ns = len <= chunk + chunk / 4 ? 1 : (len + chunk - 1) / chunk;
-        ns = std::min<int64_t>(ns, a->max_splits > 1 ? std::min(a->max_splits, kPrefillMaxSplits) : kPrefillMaxSplits);
+        int64_t ns = splits_of(len, chunk);
         if (ns <= 1) {
           P->work.push_back(it);
           continue;
