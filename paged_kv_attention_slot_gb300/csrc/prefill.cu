@@ -11,13 +11,14 @@
 // GB300 design.  One CTA = two 128-row query tiles (A and B: consecutive tokens of one request, rows
 // = (token, head) pairs of one KV head's query-head group) sharing every K/V tile, so each gathered
 // K/V byte feeds twice the tensor-core work of a single tile:
-//  * warps 8-11 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps 8-9) and V
-//    (warps 10-11) tiles of 128 keys gathered row by row through the page table with 16-byte
-//    cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the tensor core
-//    reads; two stages; each producer thread's arrival on the stage's mbarrier is posted by the
-//    hardware when its copies land (cp.async.mbarrier.arrive.noinc), so a tile is announced as
-//    soon as it is in shared memory; the MMA thread fences it into the async proxy after its wait.  (TMA tile::gather4 moves 512 bytes per instruction
-//    and measured slower here for token-granular pools.)
+//  * warps 8-11 and 13-15 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps 8,
+//    9, 13, 14) and V (warps 10, 11, 15) tiles of 128 keys gathered row by row through the page table
+//    with 16-byte cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the
+//    tensor core reads; two stages.  Each producer thread's arrival on the stage's mbarrier is posted
+//    by the hardware when its copies land (cp.async.mbarrier.arrive.noinc), so a tile is announced as
+//    soon as it is in shared memory; the MMA thread fences it into the async proxy after its wait.
+//    A warp stalls on each cp.async it issues, so the gather is spread over seven warps.  (TMA
+//    tile::gather4 moves 512 bytes per instruction and measured slower here for token-granular pools.)
 //  * warp 12 (MMA): one thread issues tcgen05.mma (kind::f16, M=128, N=128, K=16, bf16 in, fp32
 //    accumulate in TMEM) in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ..., so the
 //    tensor core works on one tile while the other tile's softmax runs.  P lives in TMEM on top of
@@ -72,14 +73,18 @@ enum {
 };
 constexpr uint32_t TMEM_COLS = 512;  // S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384), O_B [384,512)
 constexpr uint32_t TMEM_O = 256;
-constexpr int THREADS = 512;          // 4 warpgroups: softmax A, softmax B, producers, MMA (+3 idle warps)
-constexpr int PRODUCER_WARP0 = 8;     // warps 8-9 gather K, 10-11 gather V
+constexpr int THREADS = 512;          // 4 warpgroups: softmax A, softmax B, producers, MMA + producers
+constexpr int PRODUCER_WARP0 = 8;     // warps 8-11 and 13-15 gather K and V
 constexpr int MMA_WARP = 12;
+// Producer roles: K by warps 8, 9, 13, 14 and V by warps 10, 11, 15 (K is needed first, by S).
+// Every warp stalls on each cp.async it issues, so the gather of a tile is spread over all seven.
+constexpr int K_WARPS = 4, V_WARPS = 3;
 // launched at 65536 / 512 = 128 registers per thread, then rebalanced per warpgroup:
-// 2 x 128 x SOFTMAX_REGS + 2 x 128 x OTHER_REGS = 45056 + 20480 = 65536 <= 65536
-constexpr uint32_t SOFTMAX_REGS = 176;
-constexpr uint32_t OTHER_REGS = 80;
-constexpr int PRODUCER_THREADS = 64;  // per operand (K or V)
+// 2 x 128 x SOFTMAX_REGS + 2 x 128 x OTHER_REGS = 47104 + 18432 = 65536 <= 65536
+constexpr uint32_t SOFTMAX_REGS = 184;
+constexpr uint32_t OTHER_REGS = 72;
+constexpr int K_PRODUCER_THREADS = 32 * K_WARPS;
+constexpr int V_PRODUCER_THREADS = 32 * V_WARPS;
 constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 }  // namespace pf
@@ -130,8 +135,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     *abort_flag = 0;
     tc::mbar_init(BAR(B_Q), 1);
     for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(BAR(B_KF + s), PRODUCER_THREADS);
-      tc::mbar_init(BAR(B_VF + s), PRODUCER_THREADS);
+      tc::mbar_init(BAR(B_KF + s), K_PRODUCER_THREADS);
+      tc::mbar_init(BAR(B_VF + s), V_PRODUCER_THREADS);
       tc::mbar_init(BAR(B_KE + s), 1);
       tc::mbar_init(BAR(B_VE + s), 1);
     }
@@ -152,11 +157,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= PRODUCER_WARP0 && warp < PRODUCER_WARP0 + 4) {
+  if (warp >= PRODUCER_WARP0 && warp != MMA_WARP) {
     // ------------------------------------------------------------------ producers (cp.async)
     tc::reg_dealloc<OTHER_REGS>();
-    const bool is_k = warp < PRODUCER_WARP0 + 2;
-    const int pw = (warp - PRODUCER_WARP0) & 1;  // which 64-row half of the K/V tile this warp fills
+    // role: operand and index among that operand's warps; warp k of n copies the row pairs
+    // q = k, k + n, k + 2n, ... (rows 2q and 2q + 1, 16 lanes per 256-byte row)
+    const bool is_k = warp == 8 || warp == 9 || warp == 13 || warp == 14;
+    const int pw = warp == 8 || warp == 10 ? 0 : warp == 9 || warp == 11 ? 1 : warp == 13 || warp == 15 ? 2 : 3;
+    const int nw = is_k ? K_WARPS : V_WARPS;
+    const int pairs = (KT / 2 - pw + nw - 1) / nw;  // row pairs of this warp per tile
+    auto row_of = [&](int idx) -> int { return 2 * (pw + nw * (idx >> 1)) + (idx & 1); };  // idx-th row
     const char* pool = is_k ? p.k_pool : p.v_pool;
     const uint32_t s_base = is_k ? sK : sV;
     const uint32_t full0 = is_k ? BAR(B_KF) : BAR(B_VF);
@@ -193,25 +203,29 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       return page * p.page_size + (key - lp * p.page_size);
     };
     bool ok = true;
-    // slot rows of the next tile are loaded one iteration ahead so their latency overlaps the copies
-    int next_a = slot_of(w.kv_begin + pw * 64 + lane);
-    int next_b = slot_of(w.kv_begin + pw * 64 + 32 + lane);
+    // slot rows of the next tile are loaded one iteration ahead so their latency overlaps the copies;
+    // lane l holds the slots of this warp's rows l and 32 + l
+    const int nrows = 2 * pairs;
+    auto slot_idx = [&](int tile, int idx) -> int {
+      return idx < nrows ? slot_of(w.kv_begin + tile * KT + row_of(idx)) : -1;
+    };
+    int next_a = slot_idx(0, lane);
+    int next_b = slot_idx(0, 32 + lane);
     for (int j = 0; j < nkt && ok; ++j) {
       const int st = j & 1;
       const int slot_a = next_a, slot_b = next_b;
       if (j + 1 < nkt) {
-        const int key1 = w.kv_begin + (j + 1) * KT + pw * 64;
-        next_a = slot_of(key1 + lane);
-        next_b = slot_of(key1 + 32 + lane);
+        next_a = slot_idx(j + 1, lane);
+        next_b = slot_idx(j + 1, 32 + lane);
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, WAIT_LIMIT));
       if (!ok) break;
       const uint32_t dst0 = s_base + st * TILE_B + half * HALF_B;
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        const int rr = 2 * i + (lane >> 4);  // row within this warp's 64
+#pragma unroll 4
+      for (int i = 0; i < pairs; ++i) {
+        const int rr = 2 * i + (lane >> 4);  // index among this warp's rows
         const int slot = __shfl_sync(0xffffffffu, i < 16 ? slot_a : slot_b, rr & 31);
-        const int row = pw * 64 + rr;
+        const int row = row_of(rr);
         const uint32_t dst = dst0 + row * 128 + ((cc ^ (row & 7)) << 4);
         const char* src = pool + (slot >= 0 ? (int64_t)slot * p.stride_token_b + head_off + c * 16 : 0);
         cp_async16(dst, src, slot >= 0 ? 16u : 0u);
@@ -225,8 +239,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
     }
-  } else if (warp >= MMA_WARP) {
-    // ------------------------------------------------------------------ MMA issuer (warps 13-15 idle)
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------------ MMA issuer
     tc::reg_dealloc<OTHER_REGS>();
     if (warp == MMA_WARP && lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, KT, false);
@@ -339,7 +353,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       // row maximum of the raw scores (the scale is positive)
       float ma[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < KT; ++c) ma[c & 3] = fmaxf(ma[c & 3], __uint_as_float(v[c]));
+      for (int c = 0; c < KT; c += 2)  // three-input max: half the instructions
+        ma[(c >> 1) & 3] = fmax3(ma[(c >> 1) & 3], __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
       const float mx = fmaxf(fmaxf(ma[0], ma[1]), fmaxf(ma[2], ma[3])) * sc;
       float corr = 1.f;
       bool rescale = false;
@@ -351,14 +366,21 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
       // P = 2^(s * sc - m) as bf16 pairs, packed in place and stored over the scores
       const float nref = m_used == -INFINITY ? 0.f : -m_used;
-      float sa[4] = {0.f, 0.f, 0.f, 0.f};
+      // packed fp32x2 FFMA / FADD: one instruction per column pair (the MUFU ex2 stays per column)
+      const uint64_t sc2 = f2pack(sc, sc), nref2 = f2pack(nref, nref);
+      uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < KT / 2; ++c) {
-        const float p0 = ex2(fmaf(__uint_as_float(v[2 * c]), sc, nref));
-        const float p1 = ex2(fmaf(__uint_as_float(v[2 * c + 1]), sc, nref));
-        sa[c & 3] += p0 + p1;
+        const uint64_t x2 = ffma2(f2pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), sc2, nref2);
+        float x0, x1;
+        f2unpack(x2, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
         v[c] = pack_bf16(p0, p1);
       }
+      float sa[4];
+      f2unpack(sum2[0], sa[0], sa[1]);
+      f2unpack(sum2[1], sa[2], sa[3]);
       tc::tmem_st64(tS, *reinterpret_cast<const uint32_t(*)[64]>(v));
       // O_X is stable here (S_X(j) completing implies PV_X(j-1) completed), and PV_X(j) cannot start
       // before this warp signals P_X(j) below: rescale O_X now if the reference maximum moved
@@ -438,13 +460,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #undef BAR
 }
 
-// Merge of the key chunks of split prefill items: one CTA per item, thread r = row r of the item's
-// two tiles (the same (token, head) order as the prefill kernel).  m = max_s lse_s, w_s =
-// 2^(lse_s - m) / sum_s 2^(lse_s - m), o = sum_s w_s o_s; rows whose chunks saw no key get o = 0 and
-// lse = -inf.
+// Merge of the key chunks of split prefill items.  Grid (items, 8): CTA (u, y) merges columns
+// [16 y, 16 y + 16) of item u; thread r = row r of the item's two tiles (the prefill kernel's
+// (token, head) order).  m = max_s lse_s, w_s = 2^(lse_s - m) / sum_s 2^(lse_s - m), o = sum_s w_s o_s;
+// a row whose chunks saw no key gets o = 0 and lse = -inf.
+constexpr int kMergeSlices = 8;  // column slices of 16 (four float4 groups) per item
+
 __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const RunParams p, int64_t first_merge) {
   const MergeItem m = p.merge[first_merge + blockIdx.x];
   const int r = threadIdx.x;
+  const int slice = blockIdx.y;
   const int G = p.group;
   const int T = pf::ROWS / G;
   const int x = r / pf::ROWS, rr = r % pf::ROWS;
@@ -453,19 +478,19 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
   const float* lse_s = p.ppart_lse + (int64_t)m.first_slot * kPrefillItemRows + r;
   float mx = -INFINITY;
   for (int sp = 0; sp < m.num_splits; ++sp) mx = fmaxf(mx, lse_s[(int64_t)sp * kPrefillItemRows]);
-  float4 acc[32];
+  float4 acc[4];
 #pragma unroll
-  for (int c = 0; c < 32; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float sum = 0.f;
   if (mx != -INFINITY) {
     for (int sp = 0; sp < m.num_splits; ++sp) {
       const float wgt = ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
       sum += wgt;
-      if (wgt == 0.f) continue;
-      const float4* src =
-          reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) * kPrefillPartialFloats) + r;
+      const float4* src = reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) *
+                                                                          kPrefillPartialFloats) +
+                          (slice * 4) * kPrefillItemRows + r;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 4; ++c) {
         const float4 v = src[c * kPrefillItemRows];
         acc[c].x = fmaf(wgt, v.x, acc[c].x);
         acc[c].y = fmaf(wgt, v.y, acc[c].y);
@@ -477,9 +502,10 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   const int64_t row = (int64_t)(m.q_row + t);
   const int head = m.kv_head * G + g;
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D +
+                                        slice * 16);
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint4 u;
     u.x = pack_bf16(acc[2 * c].x * inv, acc[2 * c].y * inv);
     u.y = pack_bf16(acc[2 * c].z * inv, acc[2 * c].w * inv);
@@ -487,11 +513,12 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
     u.w = pack_bf16(acc[2 * c + 1].z * inv, acc[2 * c + 1].w * inv);
     dst[c] = u;
   }
-  if (p.lse) p.lse[row * p.num_qo_heads + head] = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
+  if (p.lse && slice == 0)
+    p.lse[row * p.num_qo_heads + head] = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
 }
 
 cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s) {
-  prefill_merge_kernel<<<(unsigned)count, kPrefillItemRows, 0, s>>>(p, first_merge);
+  prefill_merge_kernel<<<dim3((unsigned)count, kMergeSlices), kPrefillItemRows, 0, s>>>(p, first_merge);
   return cudaGetLastError();
 }
 
