@@ -460,16 +460,16 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #undef BAR
 }
 
-// Merge of the key chunks of split prefill items.  Grid (items, 8): CTA (u, y) merges columns
-// [16 y, 16 y + 16) of item u; thread r = row r of the item's two tiles (the prefill kernel's
-// (token, head) order).  m = max_s lse_s, w_s = 2^(lse_s - m) / sum_s 2^(lse_s - m), o = sum_s w_s o_s;
-// a row whose chunks saw no key gets o = 0 and lse = -inf.
-constexpr int kMergeSlices = 8;  // column slices of 16 (four float4 groups) per item
-
+// Merge of the key chunks of split prefill items.  Grid (items, 32 / G4): CTA (u, y) merges the G4
+// four-column groups starting at group G4 y of item u; thread r = row r of the item's two tiles (the
+// prefill kernel's (token, head) order).  m = max_s lse_s, w_s = 2^(lse_s - m) / sum_s 2^(lse_s - m),
+// o = sum_s w_s o_s; a row whose chunks saw no key gets o = 0 and lse = -inf.  Few items (a shared
+// prefix, a few long requests) take one group per CTA so that the grid still covers the SMs.
+template <int G4>
 __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const RunParams p, int64_t first_merge) {
   const MergeItem m = p.merge[first_merge + blockIdx.x];
   const int r = threadIdx.x;
-  const int slice = blockIdx.y;
+  const int g0 = blockIdx.y * G4;  // first four-column group of this CTA
   const int G = p.group;
   const int T = pf::ROWS / G;
   const int x = r / pf::ROWS, rr = r % pf::ROWS;
@@ -478,9 +478,9 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
   const float* lse_s = p.ppart_lse + (int64_t)m.first_slot * kPrefillItemRows + r;
   float mx = -INFINITY;
   for (int sp = 0; sp < m.num_splits; ++sp) mx = fmaxf(mx, lse_s[(int64_t)sp * kPrefillItemRows]);
-  float4 acc[4];
+  float4 acc[G4];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < G4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float sum = 0.f;
   if (mx != -INFINITY) {
     for (int sp = 0; sp < m.num_splits; ++sp) {
@@ -488,9 +488,9 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
       sum += wgt;
       const float4* src = reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) *
                                                                           kPrefillPartialFloats) +
-                          (slice * 4) * kPrefillItemRows + r;
+                          g0 * kPrefillItemRows + r;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < G4; ++c) {
         const float4 v = src[c * kPrefillItemRows];
         acc[c].x = fmaf(wgt, v.x, acc[c].x);
         acc[c].y = fmaf(wgt, v.y, acc[c].y);
@@ -502,23 +502,24 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   const int64_t row = (int64_t)(m.q_row + t);
   const int head = m.kv_head * G + g;
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D +
-                                        slice * 16);
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D +
+                                        g0 * 4);
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    uint4 u;
-    u.x = pack_bf16(acc[2 * c].x * inv, acc[2 * c].y * inv);
-    u.y = pack_bf16(acc[2 * c].z * inv, acc[2 * c].w * inv);
-    u.z = pack_bf16(acc[2 * c + 1].x * inv, acc[2 * c + 1].y * inv);
-    u.w = pack_bf16(acc[2 * c + 1].z * inv, acc[2 * c + 1].w * inv);
-    dst[c] = u;
-  }
-  if (p.lse && slice == 0)
+  for (int c = 0; c < G4; ++c)
+    dst[c] = make_uint2(pack_bf16(acc[c].x * inv, acc[c].y * inv), pack_bf16(acc[c].z * inv, acc[c].w * inv));
+  if (p.lse && blockIdx.y == 0)
     p.lse[row * p.num_qo_heads + head] = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
 }
 
 cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s) {
-  prefill_merge_kernel<<<dim3((unsigned)count, kMergeSlices), kPrefillItemRows, 0, s>>>(p, first_merge);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (count * 8 >= 2 * (int64_t)sms)
+    prefill_merge_kernel<4><<<dim3((unsigned)count, 8), kPrefillItemRows, 0, s>>>(p, first_merge);
+  else
+    prefill_merge_kernel<1><<<dim3((unsigned)count, 32), kPrefillItemRows, 0, s>>>(p, first_merge);
   return cudaGetLastError();
 }
 
