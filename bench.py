@@ -520,14 +520,22 @@ def next_rows_measure(device, peak_tflops, hbm):
         pre.run(st["q"], st["cache"], out=o2, lse=s2)
         pk.merge_state(o1, s1, o2, s2, out=o1, lse_out=s1)
 
+    def extend_by_fused_merge():  # the prefix pass merges into the ragged pass's state in its epilogue
+        rag.run_ragged(st["q"], st["k_new"], st["v_new"], out=o1, lse=s1)
+        pre.run(st["q"], st["cache"], out=o1, lse=s1, merge_into=True)
+
     flops = 4.0 * b.head_dim * b.num_qo_heads * _visible_pairs(b.kv_len, b.q_len)
     ms, mode = kernel_ms(extend_by_merge, reps=10, iters=5)
+    ms_fused, _ = kernel_ms(extend_by_fused_merge, reps=10, iters=5)
     out["extend_by_merge"] = {
         "workload": "prefix_extend (as the prefill line) computed as ragged + paged prefix + merge",
         "launches": 3 + (1 if pre.info()["num_merge"] else 0),
         "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
         "frac": round(flops / (ms * 1e-3) / 1e12 / peak_tflops, 4), "timing": mode,
-        "plans": {"ragged_ctas": rag.info()["num_work"], "prefix_ctas": pre.info()["num_work"]}}
+        "plans": {"ragged_ctas": rag.info()["num_work"], "prefix_ctas": pre.info()["num_work"]},
+        "fused": {"launches": 2, "ms": round(ms_fused, 4), "tflops": round(flops / (ms_fused * 1e-3) / 1e12, 2),
+                  "frac": round(flops / (ms_fused * 1e-3) / 1e12 / peak_tflops, 4),
+                  "how": "the paged prefix pass merges into the ragged pass's (o, lse) in its epilogue"}}
     del st, rag, pre, o1, o2, s1, s2
     torch.cuda.empty_cache()
 

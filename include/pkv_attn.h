@@ -240,6 +240,21 @@ int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* c
                          void* stream);
 
 /*
+ * pkv_attn_prefill_run_merge: pkv_attn_prefill_run whose result is merged into a state the caller
+ * already holds in (o, lse) -- the merge of "SGLang 源码完全拆解(八)：Attention Backend", section
+ * «extend 的两种形态», done in the epilogue instead of a separate pkv_merge_state call: a prefix-cached
+ * extend is pkv_attn_ragged_run over the new tokens (causal) into (o, lse), then this call over the
+ * cached prefix (a PKV_MODE_PREFILL plan with causal = 0).
+ *   o     device bf16 [total_tokens, num_qo_heads, 128]: on entry the held normalised outputs, on exit
+ *         the merged ones (weights e^(s - m) / sum, m the larger of the two lse).
+ *   lse   device float32 [total_tokens, num_qo_heads], required: on entry the held natural-log lse
+ *         (-inf = empty state), on exit the merged lse.
+ * Rows whose segment for this pass has no key keep their held state.  A PKV_MODE_PREFILL plan only.
+ */
+int pkv_attn_prefill_run_merge(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                               void* stream);
+
+/*
  * pkv_attn_ragged_run: attention of a PKV_MODE_RAGGED plan, K/V read from contiguous tensors (the
  * ragged wrapper's forward of "SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种
  * 形态»: the new tokens' K/V straight from this step's k / v, not through the page table).

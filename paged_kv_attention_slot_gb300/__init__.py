@@ -245,10 +245,20 @@ class Plan:
         return (out, lse) if (return_lse or lse is not None) else out
 
     def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-            return_lse: bool = False, stream=None):
-        """Attention for every planned token row; q is [total_tokens, num_qo_heads, head_dim] bf16."""
+            return_lse: bool = False, merge_into: bool = False, stream=None):
+        """Attention for every planned token row; q is [total_tokens, num_qo_heads, head_dim] bf16.
+
+        merge_into=True (prefill plans): out / lse hold a state on entry (e.g. from run_ragged over the
+        new tokens) and receive the merge of that state with this pass's (pkv_attn_prefill_run_merge)."""
         if self.mode == "ragged":
             raise ValueError("a ragged plan runs with run_ragged(q, k, v)")
+        if merge_into:
+            if self.mode not in ("prefill", "extend") or out is None or lse is None:
+                raise ValueError("merge_into needs a prefill plan and the held state in out and lse")
+            self._outputs(q, out, lse, True)
+            check(lib().pkv_attn_prefill_run_merge(self._h, q.data_ptr(), C.byref(cache.struct), out.data_ptr(),
+                                                   lse.data_ptr(), _stream_ptr(stream)))
+            return out, lse
         out, lse = self._outputs(q, out, lse, return_lse)
         if self.mode == "decode":
             fns = [lib().pkv_attn_decode_run]

@@ -695,9 +695,11 @@ namespace {
 // The prefill kernel over the plan's prefill items; `cache` is the pool (paged) or a one-token-page
 // view of the contiguous K/V tensors (ragged).
 int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* cache, void* o, float* lse,
-                void* stream) {
+                void* stream, bool merge = false) {
   int st = check_run(plan, mode, q, cache, o);
   if (st != PKV_OK) return st;
+  if (merge && !lse) return fail(PKV_EINVAL, "a merging run needs the held state's lse");
+  if (merge && plan->mode != PKV_MODE_PREFILL) return fail(PKV_EINVAL, "a merging run needs a PKV_MODE_PREFILL plan");
   const int64_t first = plan->num_decode_work, count = (int64_t)plan->work.size() - first;
   if (count == 0) return PKV_OK;
   if (cache->stride_page != (int64_t)cache->page_size * cache->stride_token)
@@ -737,6 +739,7 @@ int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* 
     if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(V) failed: " + std::to_string((int)r));
   }
   pkv::RunParams p = make_params(plan, q, cache, o, lse, first, count);
+  p.merge_into = merge ? 1 : 0;
   PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
   const int64_t nm = (int64_t)plan->merge.size() - plan->num_decode_merge;
   if (nm > 0)
@@ -750,6 +753,11 @@ extern "C" {
 int pkv_attn_prefill_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
                          void* stream) {
   return run_prefill(plan, PKV_MODE_PREFILL, q, cache, o, lse, stream);
+}
+
+int pkv_attn_prefill_run_merge(const pkv_plan* plan, const void* q, const pkv_cache* cache, void* o, float* lse,
+                               void* stream) {
+  return run_prefill(plan, PKV_MODE_PREFILL, q, cache, o, lse, stream, true);
 }
 
 int pkv_attn_ragged_run(const pkv_plan* plan, const void* q, const void* k, const void* v, void* o, float* lse,

@@ -91,6 +91,7 @@ struct RunParams {
   int32_t window_left;
   int32_t noncausal;   // prefill: 1 = every query sees all of its request's keys (0 = causal)
   int32_t ragged_kv;   // prefill: 1 = key j of request i is row page_base + j of the pools (no page table)
+  int32_t merge_into;  // prefill: 1 = merge this pass's state into the state held in (o, lse) (LSE weights)
   float scale_log2;    // sm_scale * log2(e) (* k_scale for FP8 KV)
   float out_scale;     // 1, or v_scale for FP8 KV
   int64_t num_work;

@@ -89,6 +89,30 @@ constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 }  // namespace pf
 
+// Merge of a held state (natural-log lse `s_prev`) with this pass's (`s_this`, updated in place to the
+// merged lse): the normalised weights e^(s - m) / (e^(s_prev - m) + e^(s_this - m)), m = max; two
+// empty states (-inf) give weights 0 and lse -inf.
+__device__ __forceinline__ void merge_weights(float s_prev, float& s_this, float& w_prev, float& w_this) {
+  const float m = fmaxf(s_prev, s_this);
+  if (m == -INFINITY) {
+    w_prev = w_this = 0.f;
+    return;
+  }
+  const float a = expf(s_prev - m), b = expf(s_this - m), sum = a + b;
+  w_prev = a / sum;
+  w_this = b / sum;
+  s_this = m + logf(sum);
+}
+// f[e] += w * (bf16 element e of v), for the 8 elements of a 16-byte vector
+__device__ __forceinline__ void add_scaled_bf16x8(const uint4& v, float w, float (&f)[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = fmaf(w, __uint_as_float(u[i] << 16), f[2 * i]);
+    f[2 * i + 1] = fmaf(w, __uint_as_float(u[i] & 0xffff0000u), f[2 * i + 1]);
+  }
+}
+
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, int32_t* err) {
@@ -119,7 +143,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     const int r = threadIdx.x >> 1, half = threadIdx.x & 1;
     const int x = r >> 7, rr = r & (ROWS - 1);
     const int t = x * T + rr / G, g = rr % G;
-    if (t < w.q_rows) {
+    if (t < w.q_rows && !p.merge_into) {  // merging an empty state leaves the held state unchanged
       const int64_t row = (int64_t)(w.q_row + t);
       const int head = w.kv_head * G + g;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D +
@@ -423,9 +447,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         p.ppart_lse[(int64_t)w.out_slot * kPrefillItemRows + prow] = l > 0.f ? m_used + __log2f(l) : -INFINITY;
     } else if (ok) {
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
       const int head = w.kv_head * G + g;
       const int64_t row = (int64_t)(w.q_row + t);
+      // this pass's state (o = O / l, natural-log lse); merged into the state already held by
+      // (o, lse) when the run merges (weights e^(s - m) / sum over the two states)
+      float lse_out = l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      float w_prev = 0.f, w_this = 1.f;
+      if (p.merge_into && row_valid) merge_weights(p.lse[row * p.num_qo_heads + head], lse_out, w_prev, w_this);
+      const float inv = (l > 0.f ? 1.f / l : 0.f) * w_this;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
@@ -434,16 +463,23 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         if (row_valid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv;
+            if (p.merge_into) {
+              const uint4 prev = dst[h * 4 + q];
+              add_scaled_bf16x8(prev, w_prev, f);
+            }
             uint4 u;
-            u.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-            u.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-            u.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-            u.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            u.x = pack_bf16(f[0], f[1]);
+            u.y = pack_bf16(f[2], f[3]);
+            u.z = pack_bf16(f[4], f[5]);
+            u.w = pack_bf16(f[6], f[7]);
             dst[h * 4 + q] = u;
           }
         }
       }
-      if (row_valid && p.lse) p.lse[row * p.num_qo_heads + head] = (m_used + __log2f(l)) * 0.69314718055994531f;
+      if (row_valid && p.lse) p.lse[row * p.num_qo_heads + head] = lse_out;
     } else {
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
@@ -460,16 +496,17 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 #undef BAR
 }
 
-// Merge of the key chunks of split prefill items.  Grid (items, 32 / G4): CTA (u, y) merges the G4
-// four-column groups starting at group G4 y of item u; thread r = row r of the item's two tiles (the
-// prefill kernel's (token, head) order).  m = max_s lse_s, w_s = 2^(lse_s - m) / sum_s 2^(lse_s - m),
-// o = sum_s w_s o_s; a row whose chunks saw no key gets o = 0 and lse = -inf.  Few items (a shared
-// prefix, a few long requests) take one group per CTA so that the grid still covers the SMs.
+// Merge of the key chunks of split prefill items.  Grid (items, slices): CTA (u, y) merges the
+// four-column groups [32 y / slices, 32 (y + 1) / slices) of item u, G4 at a time; thread r = row r
+// of the item's two tiles (the prefill kernel's (token, head) order).  m = max_s lse_s, w_s =
+// 2^(lse_s - m) / sum_s 2^(lse_s - m), o = sum_s w_s o_s; a row whose chunks saw no key gets o = 0 and
+// lse = -inf.  Few items (a shared prefix, a few long requests) take one group per CTA so that the
+// grid still covers the SMs.  A merging run (the result merged into the state held in (o, lse)) uses
+// one CTA per item, so that each row's held lse is read and rewritten by one thread.
 template <int G4>
 __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const RunParams p, int64_t first_merge) {
   const MergeItem m = p.merge[first_merge + blockIdx.x];
   const int r = threadIdx.x;
-  const int g0 = blockIdx.y * G4;  // first four-column group of this CTA
   const int G = p.group;
   const int T = pf::ROWS / G;
   const int x = r / pf::ROWS, rr = r % pf::ROWS;
@@ -478,37 +515,52 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
   const float* lse_s = p.ppart_lse + (int64_t)m.first_slot * kPrefillItemRows + r;
   float mx = -INFINITY;
   for (int sp = 0; sp < m.num_splits; ++sp) mx = fmaxf(mx, lse_s[(int64_t)sp * kPrefillItemRows]);
-  float4 acc[G4];
-#pragma unroll
-  for (int c = 0; c < G4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float sum = 0.f;
-  if (mx != -INFINITY) {
-    for (int sp = 0; sp < m.num_splits; ++sp) {
-      const float wgt = ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
-      sum += wgt;
-      const float4* src = reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) *
-                                                                          kPrefillPartialFloats) +
-                          g0 * kPrefillItemRows + r;
-#pragma unroll
-      for (int c = 0; c < G4; ++c) {
-        const float4 v = src[c * kPrefillItemRows];
-        acc[c].x = fmaf(wgt, v.x, acc[c].x);
-        acc[c].y = fmaf(wgt, v.y, acc[c].y);
-        acc[c].z = fmaf(wgt, v.z, acc[c].z);
-        acc[c].w = fmaf(wgt, v.w, acc[c].w);
-      }
-    }
-  }
-  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  if (mx != -INFINITY)
+    for (int sp = 0; sp < m.num_splits; ++sp) sum += ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
   const int64_t row = (int64_t)(m.q_row + t);
   const int head = m.kv_head * G + g;
-  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D +
-                                        g0 * 4);
+  // the merged state of the pieces; merged in turn into the held (o, lse) when the run merges
+  float lse_out = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
+  float w_prev = 0.f, w_this = 1.f;
+  if (p.merge_into) merge_weights(p.lse[row * p.num_qo_heads + head], lse_out, w_prev, w_this);
+  const float inv = (sum > 0.f ? 1.f / sum : 0.f) * w_this;
+  const int per_cta = 32 / gridDim.y;  // four-column groups of this CTA
+  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D);
+  for (int g0 = blockIdx.y * per_cta; g0 < (blockIdx.y + 1) * per_cta; g0 += G4) {
+    float4 acc[G4];
 #pragma unroll
-  for (int c = 0; c < G4; ++c)
-    dst[c] = make_uint2(pack_bf16(acc[c].x * inv, acc[c].y * inv), pack_bf16(acc[c].z * inv, acc[c].w * inv));
-  if (p.lse && blockIdx.y == 0)
-    p.lse[row * p.num_qo_heads + head] = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
+    for (int c = 0; c < G4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mx != -INFINITY) {
+      for (int sp = 0; sp < m.num_splits; ++sp) {
+        const float wgt = ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
+        const float4* src = reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) *
+                                                                            kPrefillPartialFloats) +
+                            g0 * kPrefillItemRows + r;
+#pragma unroll
+        for (int c = 0; c < G4; ++c) {
+          const float4 v = src[c * kPrefillItemRows];
+          acc[c].x = fmaf(wgt, v.x, acc[c].x);
+          acc[c].y = fmaf(wgt, v.y, acc[c].y);
+          acc[c].z = fmaf(wgt, v.z, acc[c].z);
+          acc[c].w = fmaf(wgt, v.w, acc[c].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < G4; ++c) {
+      float f[4] = {acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv};
+      if (p.merge_into) {
+        const uint2 prev = dst[g0 + c];
+        f[0] = fmaf(w_prev, __uint_as_float(prev.x << 16), f[0]);
+        f[1] = fmaf(w_prev, __uint_as_float(prev.x & 0xffff0000u), f[1]);
+        f[2] = fmaf(w_prev, __uint_as_float(prev.y << 16), f[2]);
+        f[3] = fmaf(w_prev, __uint_as_float(prev.y & 0xffff0000u), f[3]);
+      }
+      dst[g0 + c] = make_uint2(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]));
+    }
+  }
+  if (p.lse && blockIdx.y == 0) p.lse[row * p.num_qo_heads + head] = lse_out;
 }
 
 cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s) {
@@ -516,7 +568,9 @@ cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  if (count * 8 >= 2 * (int64_t)sms)
+  if (p.merge_into)
+    prefill_merge_kernel<4><<<dim3((unsigned)count, 1), kPrefillItemRows, 0, s>>>(p, first_merge);
+  else if (count * 8 >= 2 * (int64_t)sms)
     prefill_merge_kernel<4><<<dim3((unsigned)count, 8), kPrefillItemRows, 0, s>>>(p, first_merge);
   else
     prefill_merge_kernel<1><<<dim3((unsigned)count, 32), kPrefillItemRows, 0, s>>>(p, first_merge);

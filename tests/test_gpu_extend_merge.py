@@ -236,3 +236,48 @@ def test_split_ragged_long_kv():
     # contiguous K/V much longer than the queries: a split ragged pass
     out, lse, ro, rl = _ragged_case([12000, 64], [32, 64], 16, 4, seed=91)
     _compare_with_empty(out, lse, ro, rl)
+
+
+def extend_by_fused_merge(b, g, **prefix_kw):
+    """Two calls: ragged (new tokens, causal) into (o, lse), then the paged prefix pass merged into them."""
+    pk = _pk()
+    kw = dict(num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
+              sm_scale=b.sm_scale)
+    rag = pk.Plan().plan(b.qo_indptr, b.qo_indptr, None, None, mode="ragged", **kw)
+    pi, px, pl = prefix_csr(b)
+    pre = pk.Plan().plan(b.qo_indptr, pi, px, pl, page_size=b.page_size, mode="prefill", causal=False, **kw,
+                         **prefix_kw)
+    out, lse = rag.run_ragged(g.q, g.k_new, g.v_new, return_lse=True)
+    pre.run(g.q, g.cache, out=out, lse=lse, merge_into=True)
+    torch.cuda.synchronize()
+    return out, lse, pre
+
+
+@pytest.mark.parametrize("ps, split", [(1, False), (16, False), (16, True)])
+def test_extend_by_fused_merge_equals_single_causal_pass(ps, split):
+    # includes a request without a cached prefix (its rows keep the ragged state) and, with split,
+    # a prefix pass cut into chunks whose merge kernel merges into the held state
+    b = W.make_batch([700, 129, 64, 1000, 90], [300, 129, 1, 37, 0], ps, 32, 8, 128, seed=80 + ps)
+    g = G.GpuBatch(b)
+    g.store()
+    out, lse, pre = extend_by_fused_merge(b, g, **({"num_sms": 4096} if split else {"max_splits": 1}))
+    assert (pre.info()["num_prefill_partials"] > 0) == split
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt)
+    G.compare(out, lse, ro, rl)
+
+
+def test_extend_by_fused_merge_full_size_sampled():
+    b = W.workload(3)
+    g = G.GpuBatch(b)
+    g.store()
+    out, lse, _ = extend_by_fused_merge(b, g)
+    rng = np.random.default_rng(4)
+    rows = []
+    for i in range(b.batch_size):
+        q0, q1 = int(b.qo_indptr[i]), int(b.qo_indptr[i + 1])
+        rows += [q0, q1 - 1] + rng.integers(q0, q1, size=3).tolist()
+    rows = sorted(set(rows))
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt, rows=rows)
+    G.compare(out, lse, ro, rl, rows=rows)
