@@ -383,21 +383,30 @@ def run_e2e(b, st, plan, steps, warmup):
     import paged_kv_attention_slot_gb300 as pk
 
     kw = _plan_kw(b)
-    hq = b.q.pin_memory()
-    hk = b.k_new.pin_memory()
-    hv = b.v_new.pin_memory()
-    hs = torch.from_numpy(b.slot_mapping).pin_memory()
+    # the step's inputs (Q, the new K/V rows, slot_mapping) packed in one pinned host buffer and
+    # copied to one device buffer with a single H2D copy; the device tensors are views of it
+    parts = [b.q.contiguous().view(torch.uint8).reshape(-1), b.k_new.contiguous().view(torch.uint8).reshape(-1),
+             b.v_new.contiguous().view(torch.uint8).reshape(-1),
+             torch.from_numpy(b.slot_mapping).contiguous().view(torch.uint8).reshape(-1)]
+    offs = [0]
+    for t in parts:
+        offs.append(offs[-1] + (t.numel() + 255) // 256 * 256)
+    h_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+    for t, o in zip(parts, offs):
+        h_in[o:o + t.numel()] = t
+    d_in = torch.empty(offs[-1], dtype=torch.uint8, device=st["q"].device)
+    q = d_in[offs[0]:offs[0] + parts[0].numel()].view(torch.bfloat16).view(b.q.shape)
+    k_new = d_in[offs[1]:offs[1] + parts[1].numel()].view(torch.bfloat16).view(b.k_new.shape)
+    v_new = d_in[offs[2]:offs[2] + parts[2].numel()].view(torch.bfloat16).view(b.v_new.shape)
+    slots = d_in[offs[3]:offs[3] + parts[3].numel()].view(torch.int64)
     hout = torch.empty_like(b.q).pin_memory()
     stream = torch.cuda.current_stream()
 
     def step():
-        st["q"].copy_(hq, non_blocking=True)
-        st["k_new"].copy_(hk, non_blocking=True)
-        st["v_new"].copy_(hv, non_blocking=True)
-        st["slots"].copy_(hs, non_blocking=True)
-        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **kw)
-        pk.kv_store(st["k_new"], st["v_new"], st["slots"], st["cache"])
-        plan.run(st["q"], st["cache"], out=st["out"])
+        d_in.copy_(h_in, non_blocking=True)
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, stream=stream, **kw)
+        pk.kv_store(k_new, v_new, slots, st["cache"], stream=stream)
+        plan.run(q, st["cache"], out=st["out"], stream=stream)
         hout.copy_(st["out"], non_blocking=True)
         stream.synchronize()
 
@@ -408,7 +417,7 @@ def run_e2e(b, st, plan, steps, warmup):
     for _ in range(steps):
         step()
     dt = time.perf_counter() - t0
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs))
+    h2d = sum(t.numel() for t in parts)  # bytes of Q, K/V rows and slots (padding excluded)
     h2d += sum(a.nbytes for a in (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len))
     d2h = hout.numel() * hout.element_size()
     return dt, h2d, d2h

@@ -43,13 +43,25 @@ def library_path() -> str:
     return _lib.LIB_PATH
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_ptr(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return int(s.cuda_stream)
+    """cudaStream_t of `stream`, or of the current stream on the current device."""
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if _raw_stream is not None:  # the current stream's handle without building a Stream object
+        return int(_raw_stream(torch.cuda.current_device()))
+    return int(torch.cuda.current_stream().cuda_stream)
 
 
 def _i32(a) -> np.ndarray:
+    if isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous:
+        return a  # already what the C ABI reads: no copy
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+_EMPTY_I32 = np.zeros(1, dtype=np.int32)  # a valid address for optional arrays that are absent
 
 
 def _ptr(a: np.ndarray):
@@ -127,6 +139,11 @@ def device_error(reset: bool = True, stream=None) -> int:
     return int(code.value)
 
 
+_MODES = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL,
+          "mixed": _lib.PKV_MODE_MIXED, "ragged": _lib.PKV_MODE_RAGGED}
+_KV_DTYPES = {"bf16": _lib.PKV_BF16, "e4m3": _lib.PKV_FP8_E4M3, "fp8": _lib.PKV_FP8_E4M3}
+
+
 class Plan:
     """A reusable plan object: plan() once per batch, run() once per layer."""
 
@@ -150,15 +167,13 @@ class Plan:
     def _args(qo_indptr, kv_indptr, kv_indices, last_page_len, num_qo_heads, num_kv_heads, head_dim, page_size,
               mode, window_left, sm_scale, kv_dtype, max_splits, num_sms, causal=True):
         # ragged plans have no page table: kv_indices / last_page_len may be None
-        arrs = [_i32(qo_indptr), _i32(kv_indptr), _i32([] if kv_indices is None else kv_indices),
-                _i32([] if last_page_len is None else last_page_len)]
+        arrs = [_i32(qo_indptr), _i32(kv_indptr), _EMPTY_I32 if kv_indices is None else _i32(kv_indices),
+                _EMPTY_I32 if last_page_len is None else _i32(last_page_len)]
         B = len(arrs[0]) - 1
-        m = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL,
-             "mixed": _lib.PKV_MODE_MIXED, "ragged": _lib.PKV_MODE_RAGGED}[mode]
-        kd = {"bf16": _lib.PKV_BF16, "e4m3": _lib.PKV_FP8_E4M3, "fp8": _lib.PKV_FP8_E4M3}[kv_dtype]
-        a = _lib.pkv_plan_args(B, _ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(arrs[3]), num_qo_heads,
-                               num_kv_heads, head_dim, page_size, m, 1 if causal else 0, window_left,
-                               float(sm_scale), _lib.PKV_BF16, kd, max_splits, num_sms)
+        a = _lib.pkv_plan_args(B, arrs[0].ctypes.data, arrs[1].ctypes.data, arrs[2].ctypes.data,
+                               arrs[3].ctypes.data, num_qo_heads, num_kv_heads, head_dim, page_size, _MODES[mode],
+                               1 if causal else 0, window_left, float(sm_scale), _lib.PKV_BF16, _KV_DTYPES[kv_dtype],
+                               max_splits, num_sms)
         return a, arrs
 
     @staticmethod

@@ -59,12 +59,13 @@ _i32p = C.POINTER(C.c_int32)
 
 
 class pkv_plan_args(C.Structure):
+    # the index arrays are host addresses (const int32_t*), set from ndarray.ctypes.data
     _fields_ = [
         ("batch_size", C.c_int32),
-        ("qo_indptr", _i32p),
-        ("kv_indptr", _i32p),
-        ("kv_indices", _i32p),
-        ("last_page_len", _i32p),
+        ("qo_indptr", C.c_void_p),
+        ("kv_indptr", C.c_void_p),
+        ("kv_indices", C.c_void_p),
+        ("last_page_len", C.c_void_p),
         ("num_qo_heads", C.c_int32),
         ("num_kv_heads", C.c_int32),
         ("head_dim", C.c_int32),

@@ -635,7 +635,9 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
   }
   if (!plan->copy_done) PKV_CUDA(cudaEventCreateWithFlags(&plan->copy_done, cudaEventDisableTiming), "cudaEventCreate");
   char* h = (char*)plan->pinned;
-  std::memset(h, 0, plan->meta_bytes);
+  // the segments below are rewritten in full; only the split counters must start at zero (the
+  // alignment gaps between segments are never read)
+  std::memset(h + plan->off_count, 0, plan->meta_bytes - plan->off_count);
   std::memcpy(h + plan->off_work, plan->work.data(), plan->work.size() * sizeof(WorkItem));
   std::memcpy(h + plan->off_merge, plan->merge.data(), plan->merge.size() * sizeof(MergeItem));
   std::memcpy(h + plan->off_req, plan->req.data(), plan->req.size() * sizeof(ReqInfo));
