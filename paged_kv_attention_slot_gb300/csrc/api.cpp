@@ -67,13 +67,19 @@ int query_num_sms(int32_t requested, int32_t* out) {
     *out = requested;
     return PKV_OK;
   }
+  static int cached[64] = {0};  // SM count per device (a plan per batch asks for it every time)
   int dev = 0, n = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess && dev >= 0 && dev < 64 && cached[dev] > 0) {
+    *out = cached[dev];
+    return PKV_OK;
+  }
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess || n <= 0) {
     cudaGetLastError();
     return fail(PKV_EINVAL, "num_sms == 0 needs a visible CUDA device; pass num_sms > 0 for a host-only plan");
   }
+  if (dev >= 0 && dev < 64) cached[dev] = n;
   *out = n;
   return PKV_OK;
 }
@@ -182,19 +188,32 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     P->req[i] = ReqInfo{a->kv_indptr[i], (int32_t)L, a->qo_indptr[i], (int32_t)n};
   }
   P->indices.resize(ragged ? 0 : nnz);
-  if (!ragged && nnz) std::memcpy(P->indices.data(), a->kv_indices, nnz * sizeof(int32_t));
   if (ragged) {
     P->max_page_id = nnz - 1;  // the largest K/V row the plan reads
   } else {
-    int32_t mn = 0, mx = -1;
+    // copy the page list and find its range in one pass (four independent min / max chains)
     const int32_t* ix = a->kv_indices;
-    if (nnz) mn = mx = ix[0];
-    for (int64_t k = 0; k < nnz; ++k) {
-      mn = std::min(mn, ix[k]);
-      mx = std::max(mx, ix[k]);
+    int32_t* dst = P->indices.data();
+    int32_t mn[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX}, mx[4] = {-1, -1, -1, -1};
+    int64_t k = 0;
+    for (; k + 4 <= nnz; k += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int32_t v = ix[k + u];
+        dst[k + u] = v;
+        mn[u] = std::min(mn[u], v);
+        mx[u] = std::max(mx[u], v);
+      }
     }
-    if (mn < 0) return fail(PKV_EINVAL, "kv_indices entries must be >= 0");
-    P->max_page_id = nnz ? mx : -1;
+    for (; k < nnz; ++k) {
+      dst[k] = ix[k];
+      mn[0] = std::min(mn[0], ix[k]);
+      mx[0] = std::max(mx[0], ix[k]);
+    }
+    const int32_t lo = std::min(std::min(mn[0], mn[1]), std::min(mn[2], mn[3]));
+    const int32_t hi = std::max(std::max(mx[0], mx[1]), std::max(mx[2], mx[3]));
+    if (nnz && lo < 0) return fail(PKV_EINVAL, "kv_indices entries must be >= 0");
+    P->max_page_id = nnz ? hi : -1;
   }
 
   int32_t sms = 0;

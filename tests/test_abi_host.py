@@ -376,3 +376,16 @@ def test_prefill_split_respects_max_splits_and_many_items(pk):
     big = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=32, num_kv_heads=8,
                          head_dim=128, page_size=1, mode="prefill", num_sms=152, host_only=True)
     assert big.info()["num_prefill_partials"] == 0 and big.info()["num_merge"] == 0
+
+
+def test_prefill_run_merge_argument_checks(pk):
+    import ctypes as C
+
+    L = pk._lib.lib()
+    # a host-only plan cannot run; a decode plan cannot merge; a merging run needs the held lse
+    p = pk.Plan().plan([0, 40], [0, 3], [0, 1, 2], [16], num_qo_heads=8, num_kv_heads=2, head_dim=128,
+                       page_size=16, mode="prefill", num_sms=152, host_only=True)
+    cache = pk._lib.pkv_cache(16, 16, 4, 16, 2, 128, 0, 4096, 256, 128, 1.0, 1.0)
+    assert L.pkv_attn_prefill_run_merge(p._h, 16, C.byref(cache), 16, None, None) == pk._lib.PKV_EINVAL
+    assert L.pkv_attn_prefill_run_merge(None, 16, C.byref(cache), 16, 16, None) == pk._lib.PKV_EINVAL
+    assert "plan" in L.pkv_last_error().decode()
