@@ -131,7 +131,7 @@ def test_decode_page_sizes_and_head_dims(ps, D):
     _decode_case(b)
 
 
-@pytest.mark.parametrize("hq, hkv", [(4, 4), (8, 1), (16, 2), (32, 1), (40, 2), (64, 8)])
+@pytest.mark.parametrize("hq, hkv", [(4, 4), (8, 1), (16, 2), (32, 1), (40, 2), (64, 8), (128, 1)])
 def test_decode_gqa_groups(hq, hkv):
     lens = [5, 64, 250, 777]
     b = W.make_batch(lens, [1] * len(lens), 16, hq, hkv, 128, seed=hq * 7 + hkv)

@@ -41,8 +41,8 @@ def test_prefill_multi_tile_with_prefix():
     _case(b)
 
 
-@pytest.mark.parametrize("hq, hkv", [(4, 4), (8, 4), (8, 2), (16, 2), (32, 2)])
-def test_prefill_gqa_groups(hq, hkv):
+@pytest.mark.parametrize("hq, hkv", [(4, 4), (8, 4), (8, 2), (16, 2), (32, 2), (64, 1), (128, 1)])
+def test_prefill_gqa_groups(hq, hkv):  # up to MQA with 128 query heads: one token per 128-row tile
     b = W.make_batch([129, 50, 400], [129, 17, 260], 1, hq, hkv, 128, seed=hq + hkv)
     _case(b)
 
