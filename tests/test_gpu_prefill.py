@@ -104,3 +104,12 @@ def test_prefill_split_respects_max_splits():
     stats, plan = _case(b, num_sms=4096, max_splits=3)
     items = plan.work_items()
     assert items[:, 6].max() >= 0 and plan.info()["num_prefill_partials"] <= 3 * plan.info()["num_merge"]
+
+
+def test_prefill_long_request_sampled():
+    # maximum-size case: one request, 8192 new tokens after a 32768-token prefix (up to 320 key tiles
+    # per CTA), checked on sampled rows including the first and the last
+    b = W.make_batch([32768 + 8192], [8192], 16, 32, 8, 128, seed=83)
+    rows = sorted(set([0, 1, 63, 64, 4095, 8191] + np.random.default_rng(83).integers(0, 8192, size=6).tolist()))
+    stats, plan = _case(b, rows=rows)
+    assert plan.info()["num_work"] == 8192 // 64 * 8
