@@ -404,8 +404,9 @@ def run_e2e(b, st, plan, steps, warmup):
 
     def step():
         d_in.copy_(h_in, non_blocking=True)
-        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, stream=stream, **kw)
+        # the KV write needs no plan: the GPU stores this step's rows while the host plans
         pk.kv_store(k_new, v_new, slots, st["cache"], stream=stream)
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, stream=stream, **kw)
         plan.run(q, st["cache"], out=st["out"], stream=stream)
         hout.copy_(st["out"], non_blocking=True)
         stream.synchronize()

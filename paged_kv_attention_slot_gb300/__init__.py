@@ -64,6 +64,14 @@ def _i32(a) -> np.ndarray:
 _EMPTY_I32 = np.zeros(1, dtype=np.int32)  # a valid address for optional arrays that are absent
 
 
+def _addr(a: np.ndarray) -> int:
+    """Address of a C-contiguous array's data (the buffer route is ~4x cheaper than .ctypes.data)."""
+    try:
+        return C.addressof(C.c_int32.from_buffer(a))
+    except (TypeError, ValueError):  # read-only or empty arrays
+        return a.ctypes.data
+
+
 def _ptr(a: np.ndarray):
     return a.ctypes.data_as(C.POINTER(C.c_int32))
 
@@ -170,10 +178,9 @@ class Plan:
         arrs = [_i32(qo_indptr), _i32(kv_indptr), _EMPTY_I32 if kv_indices is None else _i32(kv_indices),
                 _EMPTY_I32 if last_page_len is None else _i32(last_page_len)]
         B = len(arrs[0]) - 1
-        a = _lib.pkv_plan_args(B, arrs[0].ctypes.data, arrs[1].ctypes.data, arrs[2].ctypes.data,
-                               arrs[3].ctypes.data, num_qo_heads, num_kv_heads, head_dim, page_size, _MODES[mode],
-                               1 if causal else 0, window_left, float(sm_scale), _lib.PKV_BF16, _KV_DTYPES[kv_dtype],
-                               max_splits, num_sms)
+        a = _lib.pkv_plan_args(B, _addr(arrs[0]), _addr(arrs[1]), _addr(arrs[2]), _addr(arrs[3]), num_qo_heads,
+                               num_kv_heads, head_dim, page_size, _MODES[mode], 1 if causal else 0, window_left,
+                               float(sm_scale), _lib.PKV_BF16, _KV_DTYPES[kv_dtype], max_splits, num_sms)
         return a, arrs
 
     @staticmethod

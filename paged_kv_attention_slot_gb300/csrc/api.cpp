@@ -89,27 +89,38 @@ inline int32_t item_share(const WorkItem& x) {
   return (x.kv_end - x.kv_begin + x.num_splits - 1) / x.num_splits;
 }
 
-// Order the work list longest first (stable counting sort on the per-CTA share, bucketed so that
-// at most 4096 buckets are used: the order is exact up to 1/4096 of the longest share).
+// Order the work list longest first (stable counting sort on the per-CTA share, bucketed: the order
+// is exact up to 1/B of the longest share, B = the number of items clamped to [64, 4096]).
 void order_longest_first(std::vector<WorkItem>& all, size_t begin, size_t end) {
   const size_t n = end - begin;
   if (n < 2) return;
   WorkItem* w = all.data() + begin;
+  // one key per item (a division each; consecutive items of one split unit share theirs)
+  thread_local std::vector<int32_t> key;
+  key.resize(n);
   int32_t maxlen = 0;
-  for (size_t i = 0; i < n; ++i) maxlen = std::max(maxlen, item_share(w[i]));
+  for (size_t i = 0; i < n; ++i) {
+    const bool same = i > 0 && w[i].kv_begin == w[i - 1].kv_begin && w[i].kv_end == w[i - 1].kv_end &&
+                      w[i].num_splits == w[i - 1].num_splits;
+    key[i] = same ? key[i - 1] : item_share(w[i]);
+    maxlen = std::max(maxlen, key[i]);
+  }
+  // about one bucket per item (at least 64, at most 4096): the prefix sum over the buckets then
+  // costs no more than the passes over the items
+  const int32_t max_buckets = (int32_t)std::min<size_t>(4096, std::max<size_t>(64, n));
   int shift = 0;
-  while ((maxlen >> shift) >= 4096) ++shift;
+  while ((maxlen >> shift) >= max_buckets) ++shift;
   const int nb = (maxlen >> shift) + 1;
   thread_local std::vector<uint32_t> count;
   thread_local std::vector<WorkItem> tmp;
   count.assign(nb + 1, 0u);
   tmp.resize(n);
   uint32_t* c = count.data();
-  const WorkItem* src = w;
-  for (size_t i = 0; i < n; ++i) ++c[nb - (item_share(src[i]) >> shift)];
+  const int32_t* k = key.data();
+  for (size_t i = 0; i < n; ++i) ++c[nb - (k[i] >> shift)];
   for (int d = 0; d < nb; ++d) c[d + 1] += c[d];
   WorkItem* dst = tmp.data();
-  for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - (item_share(src[i]) >> shift)]++] = src[i];
+  for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - (k[i] >> shift)]++] = w[i];
   std::memcpy(w, dst, n * sizeof(WorkItem));
 }
 
@@ -191,27 +202,31 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   if (ragged) {
     P->max_page_id = nnz - 1;  // the largest K/V row the plan reads
   } else {
-    // copy the page list and find its range in one pass (four independent min / max chains)
+    // copy the page list, then find its range with eight independent min / max chains
     const int32_t* ix = a->kv_indices;
-    int32_t* dst = P->indices.data();
-    int32_t mn[4] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MAX}, mx[4] = {-1, -1, -1, -1};
+    if (nnz) std::memcpy(P->indices.data(), ix, (size_t)nnz * sizeof(int32_t));
+    int32_t mn[8], mx[8];
+    for (int u = 0; u < 8; ++u) {
+      mn[u] = INT32_MAX;
+      mx[u] = -1;
+    }
     int64_t k = 0;
-    for (; k + 4 <= nnz; k += 4) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
+    for (; k + 8 <= nnz; k += 8) {
+      for (int u = 0; u < 8; ++u) {
         const int32_t v = ix[k + u];
-        dst[k + u] = v;
-        mn[u] = std::min(mn[u], v);
-        mx[u] = std::max(mx[u], v);
+        mn[u] = v < mn[u] ? v : mn[u];
+        mx[u] = v > mx[u] ? v : mx[u];
       }
     }
     for (; k < nnz; ++k) {
-      dst[k] = ix[k];
       mn[0] = std::min(mn[0], ix[k]);
       mx[0] = std::max(mx[0], ix[k]);
     }
-    const int32_t lo = std::min(std::min(mn[0], mn[1]), std::min(mn[2], mn[3]));
-    const int32_t hi = std::max(std::max(mx[0], mx[1]), std::max(mx[2], mx[3]));
+    int32_t lo = mn[0], hi = mx[0];
+    for (int u = 1; u < 8; ++u) {
+      lo = std::min(lo, mn[u]);
+      hi = std::max(hi, mx[u]);
+    }
     if (nnz && lo < 0) return fail(PKV_EINVAL, "kv_indices entries must be >= 0");
     P->max_page_id = nnz ? hi : -1;
   }
