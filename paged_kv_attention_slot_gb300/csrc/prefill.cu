@@ -27,10 +27,13 @@
 //    once PV_X(j) was issued, and "S_X(j) complete" implies "PV_X(j-1) complete".
 //  * warps 0-3 / 4-7 (softmax of tile A / B): thread r owns row r (TMEM lane r).  All 128 scores of
 //    the row come into registers with four TMEM loads and one wait; then the row maximum,
-//    p = 2^(s * scale * log2 e - m) with one FFMA + ex2, bf16 pairs packed in place and stored over
-//    the scores with one 64-column TMEM store.  Causal / window masking only on tiles that need it.  The row maximum
-//    moves lazily (only when it grows by more than 2^8; exact because numerator and denominator
-//    share it), and O is rescaled in TMEM only then.  Epilogue: O / l to bf16 rows and the LSE.
+//    p = 2^(s * scale * log2 e - m) with packed FFMA + ex2, bf16 pairs packed in place and stored
+//    over the scores in two 32-column TMEM stores.  Each half is signalled on its own barrier, so
+//    the PV MMAs over keys 0-63 start while keys 64-127 are still being exponentiated.  Causal /
+//    window masking only on tiles that need it.  The row maximum moves lazily (only when it grows
+//    by more than 2^8; exact because numerator and denominator share it), and O is rescaled in TMEM
+//    only then, before the first half is signalled.  Epilogue: O / l to bf16 rows and the LSE, or an
+//    fp32 partial of a split item.
 // Registers are rebalanced with setmaxnreg: the two softmax warpgroups take 176 per thread, the
 // producer and MMA warpgroups keep 80.  Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its own
 // copies and MMAs, frees its TMEM and exits.
@@ -59,7 +62,7 @@ constexpr int OFF_QB = OFF_QA + TILE_B;
 constexpr int OFF_K = OFF_QB + TILE_B;
 constexpr int OFF_V = OFF_K + STAGES * TILE_B;
 constexpr int OFF_BAR = OFF_V + STAGES * TILE_B;
-constexpr int NUM_BARS = 16;
+constexpr int NUM_BARS = 18;
 constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
 constexpr int SMEM_USED = OFF_ABORT + 8;
@@ -67,9 +70,10 @@ constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // room to align the base to 1024 
 enum {
   B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7,
   B_SF = 9,   // [2]: S_X(j) complete (and with it PV_X(j-1))
-  B_PF = 11,  // [2]: P_X(j) stored in TMEM by the 4 softmax warps of tile X
+  B_PF = 11,  // [2]: all of P_X(j) stored in TMEM by the 4 softmax warps of tile X
   B_OD = 13,  // [2]: the last PV_X complete
-  B_FIN = 15
+  B_FIN = 15,
+  B_PH = 16   // [2]: the first half (keys 0-63) of P_X(j) stored by the 4 softmax warps of tile X
 };
 constexpr uint32_t TMEM_COLS = 512;  // S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384), O_B [384,512)
 constexpr uint32_t TMEM_O = 256;
@@ -167,6 +171,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     for (int x = 0; x < 2; ++x) {
       tc::mbar_init(BAR(B_SF + x), 1);
       tc::mbar_init(BAR(B_PF + x), 4);
+      tc::mbar_init(BAR(B_PH + x), 4);
       tc::mbar_init(BAR(B_OD + x), 1);
     }
     tc::mbar_init(BAR(B_FIN), 1);
@@ -280,11 +285,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         }
         tc::commit(BAR(B_SF + x));
       };
-      auto issue_pv = [&](int x, int st, bool first) {  // O_x += P_x V_st, P_x from TMEM
+      // O_x += P_x V_st over key steps [k0, k1) of the tile, P_x from TMEM
+      auto issue_pv = [&](int x, int st, bool first, int k0 = 0, int k1 = KT / 16) {
         const uint32_t a0 = tmem + (uint32_t)x * 128;
         const uint32_t d = tmem + TMEM_O + (uint32_t)x * 128;
 #pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
+        for (int kk = k0; kk < k1; ++kk) {
           const uint64_t b = tc::smem_desc_sw128(sV + st * TILE_B + kk * 2048, HALF_B, 1024);
           tc::mma_bf16_ts(d, a0 + kk * 8, b, idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
@@ -304,11 +310,15 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         const int st = j & 1, st1 = (j + 1) & 1;
         const uint32_t ph = (j >> 1) & 1, ph1 = ((j + 1) >> 1) & 1;
         const bool more = j + 1 < nkt;
-        ok = wait(BAR(B_PF + 0), j & 1) && wait(BAR(B_VF + st), ph);
+        ok = wait(BAR(B_PH + 0), j & 1) && wait(BAR(B_VF + st), ph);
         if (!ok) break;
         tc::fence_proxy_async_smem();
         tc::fence_after_sync();
-        issue_pv(0, st, j == 0);
+        issue_pv(0, st, j == 0, 0, KT / 32);
+        ok = wait(BAR(B_PF + 0), j & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+        issue_pv(0, st, j == 0, KT / 32, KT / 16);
         if (more) {
           ok = wait(BAR(B_KF + st1), ph1);
           if (!ok) break;
@@ -317,10 +327,14 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           issue_s(0, st1);
         }
         if (two) {
+          ok = wait(BAR(B_PH + 1), j & 1);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(1, st, j == 0, 0, KT / 32);
           ok = wait(BAR(B_PF + 1), j & 1);
           if (!ok) break;
           tc::fence_after_sync();
-          issue_pv(1, st, j == 0);
+          issue_pv(1, st, j == 0, KT / 32, KT / 16);
           if (more) issue_s(1, st1);
         }
         tc::commit(BAR(B_VE + st));
@@ -388,40 +402,44 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         l *= corr;
         rescale = true;
       }
-      // P = 2^(s * sc - m) as bf16 pairs, packed in place and stored over the scores
+      // P = 2^(s * sc - m) as bf16 pairs, packed in place and stored over the scores in two halves:
+      // PV on keys 0-63 starts while keys 64-127 are still being exponentiated
       const float nref = m_used == -INFINITY ? 0.f : -m_used;
       // packed fp32x2 FFMA / FADD: one instruction per column pair (the MUFU ex2 stays per column)
       const uint64_t sc2 = f2pack(sc, sc), nref2 = f2pack(nref, nref);
       uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < KT / 2; ++c) {
-        const uint64_t x2 = ffma2(f2pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), sc2, nref2);
-        float x0, x1;
-        f2unpack(x2, x0, x1);
-        const float p0 = ex2(x0), p1 = ex2(x1);
-        sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
-        v[c] = pack_bf16(p0, p1);
+      for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int c = h * (KT / 4); c < (h + 1) * (KT / 4); ++c) {
+          const uint64_t x2 = ffma2(f2pack(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), sc2, nref2);
+          float x0, x1;
+          f2unpack(x2, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
+          v[c] = pack_bf16(p0, p1);
+        }
+        tc::tmem_st32(tS + h * 32, *reinterpret_cast<const uint32_t(*)[32]>(v + h * 32));
+        // O_X is stable here (S_X(j) completing implies PV_X(j-1) completed), and PV_X(j) cannot
+        // start before the first half of P_X(j) is signalled: rescale O_X now if the maximum moved
+        if (h == 0 && j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t o[32];
+            tc::tmem_ld32(tO + c4 * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+            tc::tmem_st32(tO + c4 * 32, o);
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(BAR(h == 0 ? B_PH + x : B_PF + x));
       }
       float sa[4];
       f2unpack(sum2[0], sa[0], sa[1]);
       f2unpack(sum2[1], sa[2], sa[3]);
-      tc::tmem_st64(tS, *reinterpret_cast<const uint32_t(*)[64]>(v));
-      // O_X is stable here (S_X(j) completing implies PV_X(j-1) completed), and PV_X(j) cannot start
-      // before this warp signals P_X(j) below: rescale O_X now if the reference maximum moved
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) {
-          uint32_t o[32];
-          tc::tmem_ld32(tO + c4 * 32, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-          tc::tmem_st32(tO + c4 * 32, o);
-        }
-      }
       l += (sa[0] + sa[1]) + (sa[2] + sa[3]);
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(BAR(B_PF + x));
     }
     if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD + x), 0, abort_flag, WAIT_LIMIT));
     if (ok && w.out_slot >= 0) {
