@@ -487,7 +487,7 @@ def prefill_measure(device, steps, warmup, peak_tflops):
                      "frac": round(achieved / peak_tflops, 4), "kernel_ms": round(k_ms, 4), "timing": k_mode,
                      "traffic": _traffic("prefill", PREFILL_SOURCES)},
         "run_ms_mean_in_steps": round(run_avg, 4),
-        "gpu_launches_per_step": 2,
+        "gpu_launches_per_step": 3,  # plan metadata copy + kv_store + prefill (no split items here)
     }
 
 
@@ -685,7 +685,7 @@ def main():
     run_avg = statistics.mean(run_ms)
     k_ms, k_mode = kernel_ms(lambda: plan.run(st["q"], st["cache"], out=st["out"]))
     achieved = kv_bytes / (k_ms * 1e-3) / 1e9
-    launches_per_step = 2  # kv_store + decode (the split-KV merge runs inside the decode kernel)
+    launches_per_step = 3  # plan metadata copy + kv_store + decode (the split-KV merge runs inside decode)
 
     prefill = None
     if not args.no_prefill and rank == 0:

@@ -200,8 +200,10 @@ int pkv_plan_workspace_size(const pkv_plan_args* args, size_t* bytes);
 /*
  * pkv_attn_plan: validate the batch, copy its host arrays, build the CTA work list (split-KV
  * chunks for decode, query tiles for prefill, longest first), lay out the workspace and enqueue ONE
- * host-to-device copy of the metadata from the plan's pinned staging buffer into `workspace` on
- * `stream`.  Before rewriting the staging buffer it waits for this plan object's previous copy.
+ * copy of the metadata from the plan's pinned staging buffer into `workspace` on `stream`: a small
+ * copy kernel that reads the staging buffer through its device mapping (a DMA copy where the device
+ * cannot map host memory).  Before rewriting the staging buffer it waits for this plan object's
+ * previous copy.
  * The host arrays may be reused by the caller as soon as the call returns.
  *   workspace       device, 256-byte aligned, >= pkv_plan_workspace_size() bytes; it must stay
  *                   allocated and unmodified until the last run that uses this plan has finished.

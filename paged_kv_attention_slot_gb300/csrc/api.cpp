@@ -655,6 +655,7 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
     if (plan->copy_done) cudaEventDestroy(plan->copy_done);
     cudaFreeHost(plan->pinned);
     plan->pinned = nullptr;
+    plan->pinned_dev = nullptr;
     plan->pinned_bytes = 0;
     plan->copy_done = nullptr;
   }
@@ -662,10 +663,18 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
   if (plan->pinned_bytes < plan->meta_bytes) {
     if (plan->pinned) cudaFreeHost(plan->pinned);
     plan->pinned = nullptr;
+    plan->pinned_dev = nullptr;
     size_t want = std::max<size_t>(plan->meta_bytes, 64 << 10);
     want = std::max<size_t>(want, plan->pinned_bytes * 2);
-    PKV_CUDA(cudaHostAlloc(&plan->pinned, want, cudaHostAllocDefault), "cudaHostAlloc (plan staging)");
+    // mapped, so that a kernel can read it directly (the metadata copy below)
+    PKV_CUDA(cudaHostAlloc(&plan->pinned, want, cudaHostAllocMapped), "cudaHostAlloc (plan staging)");
     plan->pinned_bytes = want;
+    int can_map = 0;
+    if (cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev) == cudaSuccess && can_map) {
+      void* d = nullptr;
+      if (cudaHostGetDevicePointer(&d, plan->pinned, 0) == cudaSuccess) plan->pinned_dev = d;
+    }
+    cudaGetLastError();  // a failed mapping query only selects the DMA copy
   }
   if (!plan->copy_done) PKV_CUDA(cudaEventCreateWithFlags(&plan->copy_done, cudaEventDisableTiming), "cudaEventCreate");
   char* h = (char*)plan->pinned;
@@ -677,7 +686,12 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
   std::memcpy(h + plan->off_req, plan->req.data(), plan->req.size() * sizeof(ReqInfo));
   std::memcpy(h + plan->off_idx, plan->indices.data(), plan->indices.size() * sizeof(int32_t));
   cudaStream_t s = (cudaStream_t)stream;
-  PKV_CUDA(cudaMemcpyAsync(workspace, h, plan->meta_bytes, cudaMemcpyHostToDevice, s), "plan metadata copy");
+  // a small kernel reading the mapped staging buffer: a DMA copy of this size spends most of its
+  // time in fixed start-up latency on the stream
+  if (plan->pinned_dev)
+    PKV_CUDA(pkv::launch_meta_copy(workspace, plan->pinned_dev, plan->meta_bytes, s), "plan metadata copy");
+  else
+    PKV_CUDA(cudaMemcpyAsync(workspace, h, plan->meta_bytes, cudaMemcpyHostToDevice, s), "plan metadata copy");
   PKV_CUDA(cudaEventRecord(plan->copy_done, s), "cudaEventRecord");
   plan->copy_pending = true;
   plan->ws = workspace;

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_stage_key[C::WARPS][C::STAGES];
 
+  pdl_wait();  // the plan's metadata copy and the KV write before this run must be complete
   const WorkItem w = p.work[blockIdx.x];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -595,8 +596,7 @@ static cudaError_t launch_decode_t(const RunParams& p, cudaStream_t s) {
   }
   int32_t* err = device_error_ptr();
   if (!err) return cudaErrorInvalidDevice;
-  decode_kernel<D, FP8, NB><<<(unsigned)p.num_work, 128, C::SMEM, s>>>(p, err);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<D, FP8, NB>, dim3((unsigned)p.num_work), dim3(128), (size_t)C::SMEM, s, p, err);
 }
 
 int decode_ctas_per_sm(int kv_dtype, int head_dim, int group) {

@@ -63,6 +63,8 @@ struct StoreParams {
 
 template <bool FP8>
 __global__ void __launch_bounds__(256) kv_store_kernel(const StoreParams p) {
+  pdl_wait();
+  pdl_launch_dependents();  // the attention run that follows may be scheduled now (it waits for us)
   const int64_t n = p.T * p.heads * p.chunks;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = i / p.chunks;  // token * heads + head
@@ -129,11 +131,8 @@ cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, 
   const int64_t n = T * p.heads * p.chunks;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  if (fp8)
-    kv_store_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(p);
-  else
-    kv_store_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return fp8 ? launch_pdl(kv_store_kernel<true>, dim3((unsigned)blocks), dim3(256), 0, s, p)
+             : launch_pdl(kv_store_kernel<false>, dim3((unsigned)blocks), dim3(256), 0, s, p);
 }
 
 }  // namespace pkv

@@ -101,4 +101,35 @@ cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* 
   return cudaGetLastError();
 }
 
+// Copy of a plan's metadata from its pinned staging buffer, read directly through the buffer's
+// device mapping (on GB300 the Grace memory is reachable over NVLink-C2C): a few CTAs with four
+// 16-byte loads in flight per thread finish well before a DMA copy of the same ~100 KB has
+// paid its fixed start-up latency.  bytes is a multiple of 16; both pointers are 16-byte aligned.
+constexpr int kMetaThreads = 256, kMetaUnroll = 4;
+__global__ void __launch_bounds__(kMetaThreads) meta_copy_kernel(uint4* dst, const uint4* src, int64_t n16) {
+  pdl_launch_dependents();
+  const int64_t base = (int64_t)blockIdx.x * (kMetaThreads * kMetaUnroll) + threadIdx.x;
+  uint4 v[kMetaUnroll];
+  // the staging buffer is written by the host before the launch, by no kernel: read it at once
+#pragma unroll
+  for (int u = 0; u < kMetaUnroll; ++u) {
+    const int64_t i = base + u * kMetaThreads;
+    if (i < n16) v[u] = src[i];
+  }
+  pdl_wait();  // an earlier kernel (a run of the previous plan) may still read the workspace
+#pragma unroll
+  for (int u = 0; u < kMetaUnroll; ++u) {
+    const int64_t i = base + u * kMetaThreads;
+    if (i < n16) dst[i] = v[u];
+  }
+}
+
+cudaError_t launch_meta_copy(void* dst, const void* src_mapped, size_t bytes, cudaStream_t s) {
+  const int64_t n16 = (int64_t)(bytes / 16);
+  if (n16 == 0) return cudaSuccess;
+  const int64_t per_cta = kMetaThreads * kMetaUnroll;
+  return launch_pdl(meta_copy_kernel, dim3((unsigned)((n16 + per_cta - 1) / per_cta)), dim3(kMetaThreads), 0, s,
+                    static_cast<uint4*>(dst), static_cast<const uint4*>(src_mapped), n16);
+}
+
 }  // namespace pkv

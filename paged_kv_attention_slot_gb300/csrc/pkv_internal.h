@@ -107,6 +107,8 @@ cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* t
                            int64_t total_tokens, cudaStream_t s);
 int prefill_supported(const char** why);
 cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s);
+// copy of plan metadata from a mapped pinned host buffer (device alias src_mapped) to the workspace
+cudaError_t launch_meta_copy(void* dst, const void* src_mapped, size_t bytes, cudaStream_t s);
 cudaError_t launch_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o,
                                float* lse, int64_t num_states, int head_dim, cudaStream_t s);
 
@@ -139,6 +141,7 @@ struct pkv_plan {
   void* ws = nullptr;
   size_t ws_bytes = 0;
   void* pinned = nullptr;
+  void* pinned_dev = nullptr;  // device alias of the staging buffer (null: copied by DMA instead)
   size_t pinned_bytes = 0;
   cudaEvent_t copy_done = nullptr;
   bool copy_pending = false;

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, int32_t* err) {
   using namespace pf;
+  pdl_wait();  // the plan's metadata copy and the KV write before this run must be complete
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base = (raw_u + 1023u) & ~1023u;
@@ -612,10 +613,9 @@ cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* t
   }
   int32_t* err = device_error_ptr();
   if (!err) return cudaErrorInvalidDevice;
-  prefill_kernel<<<(unsigned)p.num_work, pf::THREADS, pf::SMEM_ALLOC, s>>>(
-      p, *static_cast<const CUtensorMap*>(tmap_q), *static_cast<const CUtensorMap*>(tmap_k),
-      *static_cast<const CUtensorMap*>(tmap_v), err);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel, dim3((unsigned)p.num_work), dim3(pf::THREADS), (size_t)pf::SMEM_ALLOC, s, p,
+                    *static_cast<const CUtensorMap*>(tmap_q), *static_cast<const CUtensorMap*>(tmap_k),
+                    *static_cast<const CUtensorMap*>(tmap_v), err);
 }
 
 }  // namespace pkv
