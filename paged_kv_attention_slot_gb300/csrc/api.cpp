@@ -666,15 +666,20 @@ int pkv_attn_plan(pkv_plan* plan, const pkv_plan_args* args, void* workspace, si
     plan->pinned_dev = nullptr;
     size_t want = std::max<size_t>(plan->meta_bytes, 64 << 10);
     want = std::max<size_t>(want, plan->pinned_bytes * 2);
-    // mapped, so that a kernel can read it directly (the metadata copy below)
-    PKV_CUDA(cudaHostAlloc(&plan->pinned, want, cudaHostAllocMapped), "cudaHostAlloc (plan staging)");
-    plan->pinned_bytes = want;
+    // mapped, so that a kernel can read it directly (the metadata copy below); where the device
+    // cannot map host memory, plain pinned memory and a DMA copy
     int can_map = 0;
-    if (cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev) == cudaSuccess && can_map) {
+    if (cudaDeviceGetAttribute(&can_map, cudaDevAttrCanMapHostMemory, dev) != cudaSuccess) can_map = 0;
+    if (!can_map || cudaHostAlloc(&plan->pinned, want, cudaHostAllocMapped) != cudaSuccess) {
+      plan->pinned = nullptr;
+      cudaGetLastError();
+      PKV_CUDA(cudaHostAlloc(&plan->pinned, want, cudaHostAllocDefault), "cudaHostAlloc (plan staging)");
+    } else {
       void* d = nullptr;
       if (cudaHostGetDevicePointer(&d, plan->pinned, 0) == cudaSuccess) plan->pinned_dev = d;
+      cudaGetLastError();  // a failed mapping query only selects the DMA copy
     }
-    cudaGetLastError();  // a failed mapping query only selects the DMA copy
+    plan->pinned_bytes = want;
   }
   if (!plan->copy_done) PKV_CUDA(cudaEventCreateWithFlags(&plan->copy_done, cudaEventDisableTiming), "cudaEventCreate");
   char* h = (char*)plan->pinned;
