@@ -497,8 +497,11 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     if (!s_last) return;
     __threadfence();
     // Online merge over chunks of splits: the chunk's log2-sum-exps are staged in shared memory by
-    // all threads and turned into per-row weights 2^(lse_s - M) once; each thread owns float4 columns
-    // of the output and keeps 8-16 partial reads per column in flight.
+    // all threads and turned into per-row weights 2^(lse_s - M) once, one warp per row (lanes over
+    // the splits, shuffle reductions); each thread owns float4 columns of the output and keeps 8-16
+    // partial reads per column in flight.  With one column per thread and one chunk (the usual
+    // case) the first 8-16 partials are read before the weights are known, so that round trip
+    // overlaps the staging of the log2-sum-exps.
     constexpr int V4 = C::HEADS * D / 4;            // float4s of the (at most HEADS) output rows
     constexpr int PER_T = (V4 + 127) / 128;         // float4s per thread
     constexpr int SLOT4 = kDecodeRows * D / 4;      // float4s between consecutive partials
@@ -520,6 +523,12 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     }
     const float* lse_g = p.part_lse + (int64_t)mi_.first_slot * kDecodeRows;
     const float4* pm = reinterpret_cast<const float4*>(p.part_o + (int64_t)mi_.first_slot * kDecodeRows * D);
+    constexpr int PRE = C::CTAS >= 4 ? 8 : 16;  // registers: 4 resident CTAs leave ~128 per thread
+    const int npre = (n4 <= 128 && mi_.num_splits <= cap) ? min(PRE, mi_.num_splits) : 0;
+    float4 pre[PRE];
+#pragma unroll
+    for (int u = 0; u < PRE; ++u)
+      pre[u] = (u < npre && col[0] < n4) ? __ldcg(pm + (int64_t)u * SLOT4 + col[0]) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < mi_.num_splits; s0 += cap) {
       const int ns = min(cap, mi_.num_splits - s0);
       __syncthreads();
@@ -528,21 +537,29 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
         wgt[e] = r < rows ? __ldcg(lse_g + (int64_t)(s0 + sp) * kDecodeRows + r) : -INFINITY;
       }
       __syncthreads();
-      if (threadIdx.x < rows) {
-        const int r = threadIdx.x;
-        float Mc = sM[r];
-        for (int sp = 0; sp < ns; ++sp) Mc = fmaxf(Mc, wgt[sp * C::HEADS + r]);
-        const bool none = Mc == -INFINITY;            // no key seen yet: keep every weight 0
-        const float sc = none ? 1.f : ex2(sM[r] - Mc);  // 0 on the first chunk
-        float W = sW[r] * sc;
-        for (int sp = 0; sp < ns; ++sp) {
+      for (int r = warp; r < rows; r += C::WARPS) {
+        float m = -INFINITY;
+        for (int sp = lane; sp < ns; sp += 32) m = fmaxf(m, wgt[sp * C::HEADS + r]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float m_prev = sM[r];
+        const float Mc = fmaxf(m_prev, m);
+        const bool none = Mc == -INFINITY;              // no key seen yet: keep every weight 0
+        const float sc = none ? 1.f : ex2(m_prev - Mc);  // 0 on the first chunk
+        float W = 0.f;
+        for (int sp = lane; sp < ns; sp += 32) {
           const float e = none ? 0.f : ex2(wgt[sp * C::HEADS + r] - Mc);
           wgt[sp * C::HEADS + r] = e;
           W += e;
         }
-        sM[r] = Mc;
-        sW[r] = W;
-        sScale[r] = sc;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+        __syncwarp();  // every lane has read sM[r] before lane 0 rewrites it
+        if (lane == 0) {
+          sW[r] = sW[r] * sc + W;
+          sM[r] = Mc;
+          sScale[r] = sc;
+        }
       }
       __syncthreads();
 #pragma unroll
@@ -556,7 +573,20 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
         }
       }
       const float4* base = pm + (int64_t)s0 * SLOT4;
-      if (n4 <= 128)  // one column per thread (up to 4 rows of 128 dims): 16 reads in flight
+      if (npre > 0) {  // one chunk: the first npre partials are already in registers
+        if (col[0] < n4) {
+#pragma unroll
+          for (int u = 0; u < PRE; ++u) {
+            const float wv = u < npre ? wgt[u * C::HEADS + crow[0]] : 0.f;
+            acc[0].x += wv * pre[u].x;
+            acc[0].y += wv * pre[u].y;
+            acc[0].z += wv * pre[u].z;
+            acc[0].w += wv * pre[u].w;
+          }
+        }
+        merge_accumulate<1, 16, C::HEADS>(acc, col, crow, n4, base + (int64_t)npre * SLOT4, ns - npre,
+                                          wgt + npre * C::HEADS, SLOT4);
+      } else if (n4 <= 128)  // one column per thread (up to 4 rows of 128 dims): 16 reads in flight
         merge_accumulate<1, 16, C::HEADS>(acc, col, crow, n4, base, ns, wgt, SLOT4);
       else
         merge_accumulate<PER_T, 8, C::HEADS>(acc, col, crow, n4, base, ns, wgt, SLOT4);
