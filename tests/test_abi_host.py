@@ -156,6 +156,34 @@ def test_decode_partition_covers_every_key_once(pk, n):
     assert info["kv_tokens"] == int(b.kv_len.sum())
 
 
+def test_decode_order_with_more_ctas_than_buckets(pk):
+    # 1,200 requests x 8 KV heads = 9,600 CTAs: the counting sort's bucket count is clamped at 4096
+    rng = np.random.default_rng(17)
+    B, ps = 1200, 16
+    L = rng.integers(1, 5000, B)
+    pages = (L + ps - 1) // ps
+    kv_indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    idx = rng.permutation(int(kv_indptr[-1])).astype(np.int32)
+    last = (L - (pages - 1) * ps).astype(np.int32)
+    p = pk.Plan().plan(np.arange(B + 1, dtype=np.int32), kv_indptr, idx, last, num_qo_heads=32, num_kv_heads=8,
+                       head_dim=128, page_size=ps, mode="decode", num_sms=152, host_only=True)
+    items = p.work_items()
+    assert len(items) > 4096
+    sharers = {}
+    for r in items.tolist():
+        sharers[(r[0], r[1], r[2])] = sharers.get((r[0], r[1], r[2]), 0) + 1
+    ns = np.array([sharers[(r[0], r[1], r[2])] for r in items.tolist()])
+    lens = (items[:, 4] - items[:, 3] + ns - 1) // ns
+    shift = 0
+    while (int(lens.max()) >> shift) >= 4096:
+        shift += 1
+    assert np.all(np.diff(lens) < (1 << shift))
+    # every key of every (request, KV head) is read by the CTAs of its unit
+    for (req, h, g), n in list(sharers.items())[:50]:
+        rows = items[(items[:, 0] == req) & (items[:, 1] == h)]
+        assert rows[:, 3].min() == 0 and rows[:, 4].max() == L[req]
+
+
 def test_window_partition_and_no_split(pk):
     import workloads as W
 
