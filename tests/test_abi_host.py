@@ -422,3 +422,22 @@ def test_prefill_run_merge_argument_checks(pk):
     assert L.pkv_attn_prefill_run_merge(p._h, 16, C.byref(cache), 16, None, None) == pk._lib.PKV_EINVAL
     assert L.pkv_attn_prefill_run_merge(None, 16, C.byref(cache), 16, 16, None) == pk._lib.PKV_EINVAL
     assert "plan" in L.pkv_last_error().decode()
+
+
+def test_plan_from_read_only_and_non_int32_arrays(pk):
+    # the binding reads array addresses through the buffer protocol, falling back for read-only
+    # buffers; int64 / list inputs are converted: all of them must give the same plan
+    import workloads as W
+
+    b = W.workload(2, scale_batch=0.25)
+    kw = dict(num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads, head_dim=b.head_dim,
+              page_size=b.page_size, mode="decode", num_sms=152, host_only=True)
+    ref = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **kw).work_items()
+    ro = [np.array(a, dtype=np.int32) for a in (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len)]
+    for a in ro:
+        a.flags.writeable = False
+    got_ro = pk.Plan().plan(*ro, **kw).work_items()
+    got_64 = pk.Plan().plan(*[np.asarray(a, dtype=np.int64) for a in ro], **kw).work_items()
+    got_list = pk.Plan().plan(*[a.tolist() for a in ro], **kw).work_items()
+    for got in (got_ro, got_64, got_list):
+        assert np.array_equal(got, ref)
