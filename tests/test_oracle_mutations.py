@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 from oracle import attention as A
+from oracle import fp8 as F
 from oracle import metadata as M
 from tests import test_oracle_pins as P
 
@@ -70,6 +71,8 @@ MUTATIONS = {
     "no_scale": ("attend", None),
     # transposed operand: V rows taken from K
     "v_from_k": ("attend", None),
+    # log-sum-exp in log2 units where natural log is specified
+    "lse_log2": ("attend", None),
 }
 
 
@@ -88,7 +91,13 @@ def _mutated_attend(kind):
         e = np.exp(s - m)
         return (e @ K[lo:hi + 1]) / e.sum(), m + math.log(e.sum())
 
-    return {"no_scale": no_scale, "v_from_k": v_from_k}[kind]
+    def lse_log2(q, K, V, lo, hi, scale):
+        s = (K[lo:hi + 1] @ q) * scale
+        m = s.max()
+        e = np.exp(s - m)
+        return (e @ V[lo:hi + 1]) / e.sum(), m + math.log2(e.sum())
+
+    return {"no_scale": no_scale, "v_from_k": v_from_k, "lse_log2": lse_log2}[kind]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
@@ -115,3 +124,62 @@ def test_csr_with_zero_remainder_is_caught(monkeypatch):
     monkeypatch.setattr(M, "last_page_len_for", lambda L, ps: L % ps)
     with pytest.raises(AssertionError):
         P.test_vllm_worked_example_slot_mapping_and_csr()
+
+
+def test_merge_with_base2_weights_is_caught(monkeypatch):
+    def bad(o1, s1, o2, s2):
+        m = np.maximum(s1, s2)
+        w1, w2 = np.exp2(s1 - m), np.exp2(s2 - m)  # natural-log LSEs weighted as if they were log2
+        return (o1 * w1 + o2 * w2) / (w1 + w2), m + np.log(w1 + w2)
+
+    monkeypatch.setattr(A, "merge_states", bad)
+    assert not P.check_merge_closed_form()
+
+
+def test_kv_store_with_page_and_offset_swapped_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "page_and_offset", lambda slot, ps: (slot % ps, slot // ps))
+    with pytest.raises((AssertionError, IndexError)):
+        P.test_kv_store_scatter_and_padding()
+
+
+def _encode_ties_away(x):
+    """E4M3 rounding to nearest with ties away from zero (a plausible wrong rounding mode)."""
+    pos = F.decode_table()[:0x7F]  # codes 0x00..0x7E: the finite non-negative values, increasing
+    xs = np.atleast_1d(np.asarray(x, dtype=np.float64))
+    out = np.empty(xs.shape, dtype=np.uint8)
+    for i, xi in enumerate(xs.ravel()):
+        a = min(abs(xi), 448.0) if not np.isnan(xi) else 0.0
+        j = int(np.searchsorted(pos, a))
+        if j == 0:
+            c = 0
+        elif j >= len(pos):
+            c = len(pos) - 1
+        else:
+            c = j if (a - pos[j - 1]) >= (pos[j] - a) else j - 1
+        out.ravel()[i] = c | (0x80 if np.signbit(xi) else 0)
+    return out if np.ndim(x) else out[0]
+
+
+def test_fp8_ties_away_from_zero_is_caught(monkeypatch):
+    monkeypatch.setattr(F, "encode", _encode_ties_away)
+    with pytest.raises(AssertionError):
+        P.test_e4m3_ties_round_to_even_and_saturate()
+
+
+def test_fp8_without_saturation_is_caught(monkeypatch):
+    orig = F.encode
+
+    def no_sat(x):
+        a = np.abs(np.asarray(x, dtype=np.float64))
+        return np.where(a > 448.0, np.uint8(0x7F), orig(x)).astype(np.uint8)
+
+    monkeypatch.setattr(F, "encode", no_sat)
+    with pytest.raises(AssertionError):
+        P.test_e4m3_ties_round_to_even_and_saturate()
+
+
+def test_fp8_store_product_in_float64_is_caught(monkeypatch):
+    monkeypatch.setattr(F, "quantize", lambda x, scale: F.encode(np.asarray(x, dtype=np.float64) / float(scale)))
+    with pytest.raises(AssertionError):
+        P.test_quantize_rounds_the_product_in_float32()
+

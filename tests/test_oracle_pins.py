@@ -156,6 +156,24 @@ def test_quantize_rounds_the_product_in_float32():
     # relative error of e4m3 is at most 2^-4 for normal values
     big = np.abs(x) > 2.0 ** -6 * scale * 2
     assert np.all(np.abs(back[big] - x[big]) <= np.abs(x[big]) * 2.0 ** -4 + 1e-12)
+    # inputs whose float32 product lands exactly on the midpoint of two codes: there the rounding of
+    # the product decides the code (ties to even), so a product taken in another precision shows
+    d = F.decode_table()
+    ties = []
+    for c in range(0x08, 0x7E):  # consecutive normal codes c, c + 1
+        t = np.float32((d[c] + d[c + 1]) / 2.0)
+        x0 = np.float32(np.float64(t) / np.float64(inv))
+        for k in range(-4, 5):
+            xk = x0
+            for _ in range(abs(k)):
+                xk = np.nextafter(xk, np.float32(np.sign(k) * np.inf), dtype=np.float32)
+            if np.float32(xk * inv) == t:
+                ties.append((xk, c))
+                break
+    assert len(ties) > 60
+    xt = np.array([v for v, _ in ties], dtype=np.float32)
+    even = np.array([c if c % 2 == 0 else c + 1 for _, c in ties], dtype=np.uint8)
+    assert np.array_equal(F.quantize(xt, scale), even)
 
 
 def test_bf16_widening_is_exact():
