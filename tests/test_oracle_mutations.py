@@ -183,3 +183,58 @@ def test_fp8_store_product_in_float64_is_caught(monkeypatch):
     with pytest.raises(AssertionError):
         P.test_quantize_rounds_the_product_in_float32()
 
+
+
+# ---- the plan metadata (slot mapping, CSR, page tables, decode-first split): worked-example pins ----
+METADATA_MUTATIONS = {
+    # offset taken from the logical page number and vice versa
+    "slot_page_offset_swapped": ("slot_of", lambda row, pos, ps: int(row[pos % ps]) * ps + pos // ps),
+    # the new tokens are the FIRST n positions of a request instead of the last n
+    "new_tokens_first": ("slot_mapping", lambda bt, qsl, seq, ps: np.asarray(
+        [M.slot_of(bt[i], p, ps) for i in range(len(seq)) for p in range(int(qsl[i + 1] - qsl[i]))], dtype=np.int64)),
+    # page count rounded down
+    "pages_floor": ("num_pages_for", lambda L, ps: L // ps),
+    # the decode slice takes query length < threshold instead of <= threshold
+    "decode_split_strict": ("decode_first_split", None),
+    # token table sampled without the division by the page size
+    "page_table_no_divide": ("page_table_from_token_table", lambda tt, seq, ps: np.stack(
+        [np.asarray(tt[i][: int(max(seq)): ps]) for i in range(len(seq))]).astype(np.int64)),
+    # page-size-1 view gathers every token from the first page of its request
+    "ps1_view_page_blind": ("to_page_size_one", None),
+}
+
+
+def _strict_split(query_start_loc, threshold=1):
+    qlen = np.diff(np.asarray(query_start_loc, dtype=np.int64))
+    nd = int(np.sum(qlen < threshold))
+    pq = np.concatenate([[0], np.cumsum(qlen[nd:])])
+    return nd, int(qlen[:nd].sum()), len(qlen) - nd, int(qlen[nd:].sum()), pq
+
+
+def _page_blind_ps1(kv_indptr, kv_indices, last_page_len, page_size):
+    lens = M.kv_lens_from_csr(kv_indptr, last_page_len, page_size)
+    slots, indptr = [], np.zeros(len(lens) + 1, dtype=np.int64)
+    for i, L in enumerate(lens):
+        first = int(kv_indices[kv_indptr[i]])
+        slots += [first * page_size + j for j in range(int(L))]
+        indptr[i + 1] = indptr[i] + int(L)
+    return indptr, np.asarray(slots, dtype=np.int64), np.ones(len(lens), dtype=np.int64)
+
+
+METADATA_PINS = [P.test_vllm_worked_example_slot_mapping_and_csr, P.test_minisgl_printed_metadata,
+                 P.test_last_page_len_full_page_is_page_size_not_zero, P.test_to_page_size_one_matches_slot_formula]
+
+
+@pytest.mark.parametrize("name", sorted(METADATA_MUTATIONS))
+def test_metadata_pins_catch_planted_mistake(monkeypatch, name):
+    attr, fn = METADATA_MUTATIONS[name]
+    if fn is None:
+        fn = {"decode_split_strict": _strict_split, "ps1_view_page_blind": _page_blind_ps1}[name]
+    monkeypatch.setattr(M, attr, fn)
+    failed = 0
+    for pin in METADATA_PINS:
+        try:
+            pin()
+        except (AssertionError, IndexError, ValueError):
+            failed += 1
+    assert failed > 0, f"mutation {name} survived every metadata pin"
