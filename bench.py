@@ -335,6 +335,22 @@ def run_steps(b, st, plan, steps, warmup, dist_on, record_run_events=False):
     return total_ms, run_ms
 
 
+def plan_host_us(b, plan, reps=30):
+    """Median host time of one plan() call through the public API (the planner, the binding and the
+    enqueue of the metadata copy), each call after a synchronise so no GPU wait is counted."""
+    import torch
+
+    kw = _plan_kw(b)
+    ts = []
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, **kw)
+        ts.append(time.perf_counter() - t0)
+    torch.cuda.synchronize()
+    return round(statistics.median(ts) * 1e6, 1)
+
+
 def kernel_ms(run_once, reps=20, iters=7):
     """Average device time of one run launch: `reps` launches captured in one CUDA graph and replayed
     between two CUDA events on the launching stream (no host launch gaps between the kernels).  Falls
@@ -478,6 +494,7 @@ def prefill_measure(device, steps, warmup, peak_tflops):
     total_ms, _ = run_steps(b, st, plan, steps, warmup, False)
     _, run_ms = run_steps(b, st, plan, min(steps, 5), 1, False, record_run_events=True)  # diagnostic
     run_avg = statistics.mean(run_ms)
+    plan_us = plan_host_us(b, plan)
     k_ms, k_mode = kernel_ms(lambda: plan.run(st["q"], st["cache"], out=st["out"]), reps=10, iters=5)
     achieved = flops / (k_ms * 1e-3) / 1e12
     return {
@@ -492,6 +509,7 @@ def prefill_measure(device, steps, warmup, peak_tflops):
                      "traffic": _traffic("prefill", PREFILL_SOURCES)},
         "run_ms_mean_in_steps": round(run_avg, 4),
         "gpu_launches_per_step": 3,  # plan metadata copy + kv_store + prefill (no split items here)
+        "plan_host_us": plan_us,
     }
 
 
@@ -688,6 +706,7 @@ def main():
 
     _, run_ms = run_steps(b, st, plan, min(args.steps, 10), 1, False, record_run_events=True)  # diagnostic
     run_avg = statistics.mean(run_ms)
+    plan_us = plan_host_us(b, plan)
     k_ms, k_mode = kernel_ms(lambda: plan.run(st["q"], st["cache"], out=st["out"]))
     achieved = kv_bytes / (k_ms * 1e-3) / 1e9
     launches_per_step = 3  # plan metadata copy + kv_store + decode (the split-KV merge runs inside decode)
@@ -728,7 +747,8 @@ def main():
                 "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB), no flush" % (
                     2 * st["k_pool"].numel() * 2 / 1e6),
                 "parallelism": f"dp{world} (independent batches per GPU)",
-                "plan": {"ctas": info["num_work"], "merge_units": info["num_merge"], "kv_chunk": info["kv_chunk"]},
+                "plan": {"ctas": info["num_work"], "merge_units": info["num_merge"], "kv_chunk": info["kv_chunk"],
+                         "host_us": plan_us},
             },
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src,
