@@ -763,7 +763,7 @@ int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* 
     return fail(PKV_EUNSUPPORTED, "prefill needs the heads of a token contiguous (stride_head == head_dim)");
   auto encode = get_encode_tiled();
   if (!encode) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled is unavailable");
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq;
   // Q: 3-D (head_dim, num_qo_heads, tokens), box (64, group, 128 / group), 128-byte swizzle
   {
     const int G = plan->Hq / plan->Hkv;
@@ -776,23 +776,12 @@ int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(Q) failed: " + std::to_string((int)r));
   }
-  // K/V: 2-D (num_kv_heads * head_dim columns, num_pages * page_size slot rows), box (64, 1) for gather4
-  {
-    const int64_t rows = cache->num_pages * (int64_t)cache->page_size;
-    cuuint64_t dims[2] = {(cuuint64_t)cache->num_kv_heads * cache->head_dim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cache->stride_token * 2};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t es[2] = {1, 1};
-    if (rows > INT32_MAX) return fail(PKV_EUNSUPPORTED, "prefill needs num_pages * page_size < 2^31");
-    CUresult r = encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cache->k, dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(K) failed: " + std::to_string((int)r));
-    r = encode(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cache->v, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(V) failed: " + std::to_string((int)r));
-  }
+  // the slot rows the kernel computes are 32-bit
+  if (cache->num_pages * (int64_t)cache->page_size > INT32_MAX)
+    return fail(PKV_EUNSUPPORTED, "prefill needs num_pages * page_size < 2^31");
+  // K/V are gathered with cp.async through the page table: the kernel's K/V tensor-map parameters
+  // are not read, and are passed zeroed
+  alignas(64) CUtensorMap tk{}, tv{};
   pkv::RunParams p = make_params(plan, q, cache, o, lse, first, count);
   p.merge_into = merge ? 1 : 0;
   PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
