@@ -351,7 +351,7 @@ int pkv_plan_info_get(const pkv_plan* plan, pkv_plan_info* info);
  * [kv_begin, kv_end), a whole number of 128-key tiles except at the end of the item's range; the
  * prefill run merges the pieces of each item with a second kernel.  A decode CTA with
  * out_slot = -1 reads all of [kv_begin, kv_end); the CTAs with consecutive partial slots of one
- * (request, kv_head, head_group) share the same [kv_begin, kv_end) and divide its 64-key groups
+ * (request, kv_head, head_group) share the same [kv_begin, kv_end) and divide its 32-key groups
  * among themselves at run time (each warp starts on its own group, then takes the next unclaimed
  * one from a counter in the workspace).  `capacity` is in int32. */
 int pkv_plan_work_items(const pkv_plan* plan, int32_t* out, int64_t capacity);
