@@ -106,7 +106,7 @@ def test_run_on_host_only_plan_fails_loudly(pk):
 def _check_decode_cover(b, items, window=-1, group=None):
     """Every (request, kv head, head group) has its whole visible key range [lo, L) planned exactly once:
     either one CTA reading it alone (no partial slot), or several CTAs that share it (they claim its
-    64-key groups at run time) with consecutive partial slots."""
+    32-key groups at run time) with consecutive partial slots."""
     G = group
     groups = (G + 15) // 16
     seen = {}
@@ -441,3 +441,84 @@ def test_plan_from_read_only_and_non_int32_arrays(pk):
     got_list = pk.Plan().plan(*[a.tolist() for a in ro], **kw).work_items()
     for got in (got_ro, got_64, got_list):
         assert np.array_equal(got, ref)
+
+
+def _random_batch(rng, mode):
+    """A random CSR batch for the planner fuzz test: lengths, pages, a random page permutation."""
+    B = int(rng.integers(1, 25))
+    ps = int(rng.choice([1, 4, 16, 64]))
+    if mode == "decode":
+        n = rng.choice([0, 1, 1, 1], B)
+    elif mode == "prefill":
+        n = rng.integers(1, 300, B)
+    else:
+        n = np.where(rng.random(B) < 0.5, 1, rng.integers(2, 300, B))
+    L = n + rng.integers(0, 700, B)
+    L = np.where((n == 0) & (rng.random(B) < 0.3), 0, L)
+    pages = (L + ps - 1) // ps
+    kv_indptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int32)
+    idx = rng.permutation(int(kv_indptr[-1]) + 5)[: int(kv_indptr[-1])].astype(np.int32)
+    last = np.where(pages > 0, L - (pages - 1) * ps, 1).astype(np.int32)
+    qo = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    return qo, kv_indptr, idx, last, ps, n.astype(np.int64), L.astype(np.int64)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_planner_fuzz_partitions(pk, seed):
+    """Random batches, modes, head ratios, windows, SM counts and split caps: every visible key range
+    is planned exactly once (decode units: one CTA or CTAs sharing the range with consecutive slots;
+    prefill items: pieces that tile the item's range with consecutive slots) and every new token row
+    is covered exactly once."""
+    rng = np.random.default_rng(9000 + seed)
+    mode = ["decode", "prefill", "mixed"][seed % 3]
+    qo, kv_indptr, idx, last, ps, n, L = _random_batch(rng, mode)
+    hkv = int(rng.choice([1, 2, 8]))
+    G = int(rng.choice([1, 4, 8, 16, 32]))
+    window = -1 if rng.random() < 0.5 else int(rng.integers(0, 400))
+    p = pk.Plan().plan(qo, kv_indptr, idx, last, num_qo_heads=hkv * G, num_kv_heads=hkv, head_dim=128,
+                       page_size=ps, mode=mode, window_left=window, num_sms=int(rng.choice([8, 40, 152])),
+                       max_splits=int(rng.choice([0, 1, 3])), host_only=True)
+    info = p.info()
+    items = p.work_items()
+    nd = info["num_decode_work"]
+    assert info["num_work"] == len(items)
+    is_decode = (n == 1) if mode != "prefill" else np.zeros(len(n), dtype=bool)
+    # decode units
+    groups = (G + 15) // 16
+    seen = {}
+    for req, h, hg, k0, k1, q_row, slot, q_rows in items[:nd].tolist():
+        assert is_decode[req] and q_rows == 1 and q_row == qo[req]
+        seen.setdefault((req, h, hg), []).append((k0, k1, slot))
+    for i in np.nonzero(is_decode)[0].tolist():
+        lo = max(0, int(L[i]) - 1 - window) if window >= 0 else 0
+        for h in range(hkv):
+            for hg in range(groups):
+                ranges = seen.pop((i, h, hg))
+                assert all((k0, k1) == (lo, int(L[i])) for k0, k1, _ in ranges)
+                slots = sorted(r[2] for r in ranges)
+                assert slots == [-1] if len(ranges) == 1 else slots == list(range(slots[0], slots[0] + len(slots)))
+    assert not seen
+    # prefill items: group the pieces of each (request, KV head, first row)
+    pieces = {}
+    for req, h, hg, k0, k1, q_row, slot, q_rows in items[nd:].tolist():
+        assert not is_decode[req] and n[req] > 0 and 0 < q_rows <= 2 * (128 // G)
+        pieces.setdefault((req, h, q_row, q_rows), []).append((k0, k1, slot))
+    rows = {}
+    for (req, h, q_row, q_rows), rs in pieces.items():
+        t0 = q_row - int(qo[req])
+        P0 = int(L[req] - n[req]) + t0
+        lo = max(0, P0 - window) if window >= 0 else 0
+        hi = P0 + q_rows  # the last row's position + 1 (causal)
+        rs.sort()
+        assert rs[0][0] == lo and rs[-1][1] == hi
+        assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))  # the pieces tile [lo, hi)
+        slots = [r[2] for r in rs]
+        assert slots == [-1] if len(rs) == 1 else slots == list(range(slots[0], slots[0] + len(slots)))
+        rows.setdefault((req, h), []).append((q_row, q_rows))
+    for i in np.nonzero((~is_decode) & (n > 0))[0].tolist():
+        for h in range(hkv):
+            spans = sorted(rows.pop((i, h)))
+            assert spans[0][0] == qo[i] and sum(r for _, r in spans) == n[i]
+            assert all(a[0] + a[1] == b[0] for a, b in zip(spans, spans[1:]))
+    assert not rows
+
