@@ -522,3 +522,35 @@ def test_planner_fuzz_partitions(pk, seed):
             assert all(a[0] + a[1] == b[0] for a, b in zip(spans, spans[1:]))
     assert not rows
 
+
+
+def test_binding_rejects_malformed_pools_and_kv_writes(pk):
+    # the binding's own checks, raised before any call into the library (no GPU needed)
+    import torch
+
+    ok = torch.zeros((4, 16, 2, 128), dtype=torch.bfloat16)
+    pk.KVCache(ok, ok.clone())  # well-formed
+    pk.KVCache(ok.to(torch.uint8), ok.to(torch.uint8), 0.5, 0.25)  # FP8 codes with scales
+    bad = [
+        (ok[0], ok[0]),                                            # not 4-D
+        (ok, ok[:, :8]),                                           # shapes differ
+        (ok.transpose(2, 3), ok.transpose(2, 3)),                  # head_dim not contiguous
+        (ok.float(), ok.float()),                                  # unsupported dtype
+        (ok, ok.to(torch.uint8)),                                  # K and V dtypes differ
+        (ok, torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16).transpose(1, 2)),  # strides differ
+    ]
+    for k, v in bad:
+        with pytest.raises(ValueError):
+            pk.KVCache(k, v)
+    cache = pk.KVCache(ok, ok.clone())
+    k = torch.zeros((3, 2, 128), dtype=torch.bfloat16)
+    slots = torch.zeros(3, dtype=torch.int64)
+    for args in [
+        (k.float(), k, slots),                                     # not bf16
+        (k.transpose(0, 1).contiguous().transpose(0, 1), k, slots),  # not contiguous
+        (k, k, slots.int()),                                       # slot_mapping not int64
+        (k, k, slots[:2]),                                         # one slot per token
+        (k[:, :1], k[:, :1], slots),                               # heads do not match the pool
+    ]:
+        with pytest.raises(ValueError):
+            pk.kv_store(*args, cache)
