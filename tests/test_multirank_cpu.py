@@ -41,7 +41,7 @@ def _worker(rank, world, port, out):
 def test_two_ranks_shard_batches_and_reduce_time():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this (multi-threaded) process
     out = mgr.dict()
     mp.start_processes(_worker, args=(world, port, out), nprocs=world, join=True, start_method="spawn")
     (m0, b0, g0, n0), (m1, b1, g1, n1) = out[0], out[1]
