@@ -554,3 +554,23 @@ def test_binding_rejects_malformed_pools_and_kv_writes(pk):
     ]:
         with pytest.raises(ValueError):
             pk.kv_store(*args, cache)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_host_helpers_match_the_oracle_on_random_tables(pk, seed):
+    from oracle import metadata as M
+
+    rng = np.random.default_rng(300 + seed)
+    B = int(rng.integers(1, 12))
+    ps = int(rng.choice([1, 2, 16, 64]))
+    seq = rng.integers(0, 500, B)
+    max_pages = int(max(1, ((seq + ps - 1) // ps).max()))
+    bt = rng.integers(0, 10_000, (B, max_pages + int(rng.integers(0, 3)))).astype(np.int32)
+    got = pk.block_table_to_csr(bt, seq, ps)
+    want = M.csr_from_block_table(bt, seq, ps)
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
+    has = (seq > 0)
+    assert np.array_equal(np.asarray(got[2])[has], np.asarray(want[2])[has])  # a request of length 0 has no page
+    if seq.max() > 0:
+        tt = rng.integers(0, 1 << 20, (B, int(seq.max()) + int(rng.integers(0, 4)))).astype(np.int32)
+        assert np.array_equal(pk.token_table_to_page_table(tt, seq, ps), M.page_table_from_token_table(tt, seq, ps))
