@@ -35,6 +35,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e nominal, reported beside the measured-copy fraction
 DEFAULT_BF16_TFLOPS = 1900.0
 
 
@@ -136,41 +137,50 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------------
 # CPU oracle baseline (spawned process pool; one task = one request)
 # ------------------------------------------------------------------------------------------------
-_WORKER_BATCH = None
+_WORKER_BATCHES = None
 
 
-def _oracle_worker_init(workload_n, seed_offset):
-    """Each worker regenerates the seeded batch once (untimed), so tasks carry only request ids."""
-    global _WORKER_BATCH
+def _oracle_worker_init(workload_ns, seed_offset):
+    """Each worker regenerates the seeded batches once (untimed), so tasks carry only row ids."""
+    global _WORKER_BATCHES
     import numpy as np
     import torch
 
     import workloads as W
 
-    b = W.workload(workload_n, seed_offset=seed_offset)
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
-    _WORKER_BATCH = (b, bits(b.q), bits(b.k_pool), bits(b.v_pool))
+    from oracle import attention as OA
+
+    _WORKER_BATCHES = {}
+    for n in workload_ns:
+        b = W.workload(n, seed_offset=seed_offset)
+        kb, vb = bits(b.k_pool), bits(b.v_pool)
+        if b.q_len.max() > 1:  # the prefill workload reads this step's new rows: the pool after its KV write
+            kb, vb = kb.copy(), vb.copy()
+            OA.kv_store(kb, vb, bits(b.k_new), bits(b.v_new), b.slot_mapping, b.page_size)
+        _WORKER_BATCHES[n] = (b, bits(b.q), kb, vb)
 
 
 def _noop(_):
-    return _WORKER_BATCH is not None
+    return _WORKER_BATCHES is not None
 
 
-def _oracle_request_task(i):
-    """Worker: the oracle, as it stands, on request i of the batch (its one query token)."""
+def _oracle_rows_task(task):
+    """Worker: the oracle, as it stands, on the given token rows of workload n (one request's rows)."""
     import numpy as np
 
     from oracle import attention as OA
 
-    b, qb, kb, vb = _WORKER_BATCH
+    n, rows = task
+    b, qb, kb, vb = _WORKER_BATCHES[n]
     o, _ = OA.paged_attention(qb, kb, vb, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, b.page_size,
                               sm_scale=b.sm_scale if b.sm_scale > 0 else None, window_left=b.window_left,
-                              q_format="bf16_bits", kv_format="bf16_bits", rows=[int(b.qo_indptr[i])])
+                              q_format="bf16_bits", kv_format="bf16_bits", rows=list(rows))
     return float(np.nansum(o))
 
 
 class OraclePool:
-    def __init__(self, workload_n=2, seed_offset=0):
+    def __init__(self, workload_ns=(2,), seed_offset=0):
         import multiprocessing as mp
 
         self.cores = max(1, os.cpu_count() or 1)
@@ -179,7 +189,7 @@ class OraclePool:
         os.environ.update(env)
         try:
             self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_worker_init,
-                                                     initargs=(workload_n, seed_offset))
+                                                     initargs=(tuple(workload_ns), seed_offset))
         finally:
             for k, v in old.items():
                 if v is None:
@@ -192,10 +202,14 @@ class OraclePool:
         with the GPU timing for host cores."""
         self.pool.map(_noop, range(4 * self.cores), chunksize=1)
 
-    def run(self, b, req_ids):
-        """Wall time of the oracle over these requests, one request per task."""
+    def run(self, b, req_ids, n=2):
+        """Wall time of the oracle over these decode requests (workload n), one request per task."""
+        return self.run_rows(n, [[int(b.qo_indptr[i])] for i in req_ids])
+
+    def run_rows(self, n, row_groups):
+        """Wall time of the oracle over these groups of token rows of workload n, one group per task."""
         t0 = time.perf_counter()
-        self.pool.map(_oracle_request_task, list(req_ids), chunksize=1)
+        self.pool.map(_oracle_rows_task, [(n, list(g)) for g in row_groups], chunksize=1)
         return time.perf_counter() - t0
 
     def close(self):
@@ -226,6 +240,59 @@ def cpu_baseline(b, pool, target_s=12.0):
             "sample": f"{reps} x the full {b.batch_size}-request batch ({_kv_bytes(b, ids) / 1e6:.1f} MB of KV each), "
                       f"one request per task on a spawn pool of {pool.cores} single-threaded processes, "
                       f"fp64 numpy oracle as it stands, wall clock"}
+
+
+def prefill_sample_rows(b, per_request=128, chunk=32, seed=3):
+    """A bounded, seeded sample of the prefill workload's token rows: up to `per_request` rows of
+    every request (its first and last row included), grouped by request in chunks of `chunk` rows."""
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    groups = []
+    for i in range(b.batch_size):
+        q0, q1 = int(b.qo_indptr[i]), int(b.qo_indptr[i + 1])
+        if q1 == q0:
+            continue
+        rows = np.arange(q0, q1) if q1 - q0 <= per_request else np.unique(np.concatenate(
+            [[q0, q1 - 1], rng.choice(np.arange(q0 + 1, q1 - 1), per_request - 2, replace=False)]))
+        groups += [rows[k:k + chunk].tolist() for k in range(0, len(rows), chunk)]
+    return groups
+
+
+def _rows_flops(b, row_groups):
+    """Algorithmic FLOPs of the sampled rows: 4 * D * Hq * visible keys of each row (causal)."""
+    import numpy as np
+
+    req = np.searchsorted(b.qo_indptr, np.arange(int(b.qo_indptr[-1])), side="right") - 1
+    total = 0.0
+    for g in row_groups:
+        for r in g:
+            i = int(req[r])
+            pos = int(b.kv_len[i]) - int(b.q_len[i]) + (r - int(b.qo_indptr[i]))
+            lo = 0 if b.window_left < 0 else max(0, pos - b.window_left)
+            total += 4.0 * b.head_dim * b.num_qo_heads * (pos - lo + 1)
+    return total
+
+
+def cpu_baseline_prefill(pool, target_s=10.0):
+    """The oracle, as it stands, on a bounded sample of the prefill workload's rows, TFLOP/s."""
+    import workloads as W
+
+    b = W.workload(3)
+    groups = prefill_sample_rows(b)
+    pool.run_rows(3, groups[:2])  # warm the workers
+    reps, total_t = 0, 0.0
+    while total_t < target_s and reps < 50:
+        total_t += pool.run_rows(3, groups)
+        reps += 1
+    flops = _rows_flops(b, groups)
+    nrows = sum(len(g) for g in groups)
+    return {"value": round(flops * reps / total_t / 1e12, 6), "unit": "TFLOP/s", "cores": pool.cores,
+            "kind": "oracle",
+            "sample": f"{reps} x {nrows} token rows of the prefix_extend batch (up to 128 seeded rows per request, "
+                      f"first and last included, all 32 heads; {flops / 1e9:.1f} GFLOP of visible pairs per pass), "
+                      f"{len(groups)} tasks of one request's rows on a spawn pool of {pool.cores} single-threaded "
+                      f"processes, fp64 numpy oracle as it stands, wall clock"}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -463,7 +530,8 @@ def decode_other_configs(device, hbm):
         k_ms, mode = kernel_ms(lambda: plan.run(st["q"], st["cache"], out=st["out"]))
         gbs = b.kv_bytes_read() / (k_ms * 1e-3) / 1e9
         res.append({"workload": name, "kv_bytes": b.kv_bytes_read(), "kernel_ms": round(k_ms, 4),
-                    "achieved": round(gbs, 2), "unit": "GB/s", "frac": round(gbs / hbm, 4), "timing": mode,
+                    "achieved": round(gbs, 2), "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                    "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "timing": mode,
                     "traffic": _traffic(key, DECODE_SOURCES),
                     "plan": {"ctas": info["num_work"], "merge_units": info["num_merge"], "kv_chunk": info["kv_chunk"]}})
         del st, plan
@@ -674,7 +742,8 @@ def main():
     import workloads as W
 
     # the oracle pool is spawned before the first GPU call
-    pool = OraclePool(2, 0) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    pool = OraclePool((2,) if args.no_prefill else (2, 3), 0) if (
+        rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     if pool is not None:
         pool.wait_ready()
 
@@ -724,6 +793,8 @@ def main():
     cpu = None
     if pool is not None:
         cpu = cpu_baseline(b, pool)
+        if prefill is not None and "unavailable" not in prefill:
+            prefill["cpu_baseline"] = cpu_baseline_prefill(pool)
         pool.close()
 
     if rank == 0:
@@ -752,6 +823,7 @@ def main():
             },
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                         "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                          "kernel": "decode_kernel (split-KV merge fused), one launch per decode_run",
                          "kernel_ms": round(k_ms, 4), "timing": k_mode,
                          "run_ms_mean_in_steps": round(run_avg, 4),
@@ -776,7 +848,7 @@ def reference_arm(args, world, rank):
         return
     import workloads as W
 
-    pool = OraclePool(2, 0)
+    pool = OraclePool((2,), 0)
     pool.wait_ready()
     b = W.workload(2)
     ids = list(range(b.batch_size))

@@ -60,8 +60,8 @@ typedef enum {
   PKV_MODE_MIXED = 2,   /* both in one batch: requests with one new token are planned for the
                          * decode kernel, requests with more for the prefill kernel, and the two
                          * runs write their rows of one output (the decode / prefill-extend split
-                         * of "vLLM Attention 后端与 FlashInfer 元数据", sections «为什么先把 Decode 移到前面»
-                         * and «FlashInfer Builder 的结果»).  Requests may come in any order: every
+                         * of "vLLM 源码完全拆解（六）：Attention Backend", sections «为什么先把 Decode
+                         * 移到前面» and «FlashInfer Builder 的结果»).  Requests may come in any order: every
                          * CTA carries its own token row, so no decode-first reordering is needed. */
   PKV_MODE_RAGGED = 3   /* prefill / extend over CONTIGUOUS K/V tensors instead of the paged pool
                          * (the ragged form of "SGLang 源码完全拆解(八)：Attention Backend", section
@@ -291,9 +291,9 @@ int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const 
  * (The pages have no counterpart: this entry point is an addition of this library.)
  *
  * Who needs it: code that is not allowed to call cudaMalloc -- a host framework whose memory pool
- * forbids raw allocations, a caller in the middle of building a CUDA graph, or an embedded runtime
- * that receives a fixed device-memory budget up front -- and therefore cannot provide the plan
- * workspace.  This call needs no workspace: the plan's metadata (work list, per-request facts,
+ * forbids raw allocations (an allocation made behind the pool's back breaks its accounting and its
+ * out-of-memory handling), or an embedded runtime that receives a fixed device-memory budget up
+ * front -- and therefore cannot provide the plan workspace.  This call needs no workspace: the plan's metadata (work list, per-request facts,
  * page list) and the split-KV partial outputs live in one statically sized device array inside the
  * library (32 MiB per device that loads the library, held until the process exits).  The caller
  * still passes Q, the cache and the outputs, exactly as for pkv_attn_decode_run.
@@ -301,9 +301,10 @@ int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const 
  *   plan   a PKV_MODE_DECODE plan; a host-only plan (pkv_attn_plan with workspace == NULL) is
  *          enough, and its workspace, if any, is not used.  Its pkv_plan_info().workspace_bytes
  *          must not exceed 32 MiB, otherwise PKV_EWORKSPACE is returned and nothing runs.
- * Same kernels, outputs and error checks as pkv_attn_decode_run.  The call itself allocates no
- * device or pinned memory: it copies the plan's metadata from its host arrays into the static
- * array on `stream`, then launches the kernels.
+ * Same kernels and outputs as pkv_attn_decode_run, and the same checks of the cache against the
+ * plan (geometry, page range, 16-byte alignment, positive strides, FP8 scales).  The call itself
+ * allocates no device or pinned memory: it copies the plan's metadata from the plan's (pageable)
+ * host arrays into the static array on `stream`, then launches the kernels.
  * Every call shares the one array per device and it keeps the last call's contents; calls whose
  * work may overlap on the GPU (other streams, other threads) race on it and must be serialised by
  * the caller.  The first call on a device looks up the array's device address; make that first
@@ -322,6 +323,27 @@ const char* pkv_last_error(void);
  * PKV_DEVERR_* value; the first error recorded wins) and clear it when reset != 0.  Returns
  * PKV_EDEVICE when *code != 0. */
 int pkv_device_error(int32_t* code, int32_t reset, void* stream);
+
+/*
+ * pkv_set_wait_limit: the bound on each wait inside the prefill kernel (a K/V tile, a score block,
+ * the probabilities of the softmax warps), in SM clock cycles, for every prefill, ragged and
+ * merging run launched after the call by any thread of the process; clock_cycles <= 0 restores the
+ * default of 4e9 (about 2 s).  The pages ask that failures be loud, never silent ("vLLM 源码完全拆解
+ * （六）：Attention Backend", section «自动选择与手工指定语义不同»): a wait that runs out makes its CTA
+ * record PKV_DEVERR_TIMEOUT in the device error word, wait (with a fixed bound of 5e8 cycles) for the
+ * copies and MMAs it already issued, free its tensor memory and exit without writing its rows; the
+ * error is read with pkv_device_error.  The decode kernel has no such waits.
+ * Returns PKV_EINVAL when clock_cycles exceeds 2^41.
+ */
+int pkv_set_wait_limit(int64_t clock_cycles);
+
+/*
+ * pkv_test_hold_wait: a testing aid for the timeout path above.  While `on` is nonzero, every prefill
+ * CTA launched afterwards first waits on a barrier that nothing arrives at; the wait runs out after
+ * the current wait limit and the CTA takes the timeout path (PKV_DEVERR_TIMEOUT, no output rows).
+ * Nothing faults or hangs: the held wait is bounded like every other.  No counterpart on the pages.
+ */
+int pkv_test_hold_wait(int32_t on);
 
 typedef struct pkv_plan_info {
   int32_t mode;

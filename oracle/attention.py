@@ -217,27 +217,6 @@ def paged_attention(
     return o, lse
 
 
-def paged_attention_heads(q_rows, K, V, positions, scale: float, window_left: int = -1):
-    """Same definition, one request and one KV head at a time, for many query rows.
-
-    q_rows: [n, G, D]; K, V: [L, D]; positions: [n].  Used by large parity
-    cases and the CPU baseline; identical arithmetic to ``attend`` but with the
-    score matrix formed by one matmul (a library primitive) per request/head.
-    """
-    s = np.einsum("ngd,ld->ngl", q_rows, K) * scale
-    j = np.arange(K.shape[0])
-    pos = np.asarray(positions)[:, None, None]
-    keep = j[None, None, :] <= pos
-    if window_left >= 0:
-        keep &= j[None, None, :] >= pos - window_left
-    s = np.where(keep, s, -np.inf)
-    m = s.max(axis=-1, keepdims=True)
-    e = np.exp(s - m)
-    den = e.sum(axis=-1)
-    o = np.einsum("ngl,ld->ngd", e, V) / den[..., None]
-    return o, m[..., 0] + np.log(den)
-
-
 def kv_rows_of(kv_indptr, i: int):
     """Rows [begin, end) of the contiguous K/V tensors that request i owns."""
     return int(kv_indptr[i]), int(kv_indptr[i + 1])

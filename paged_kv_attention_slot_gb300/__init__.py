@@ -147,6 +147,13 @@ def device_error(reset: bool = True, stream=None) -> int:
     return int(code.value)
 
 
+def set_wait_limit(clock_cycles: int = 0) -> None:
+    """Bound, in SM clock cycles, on each wait inside the prefill kernel for runs launched from now
+    on (0 restores the default, about 2 s).  A wait that runs out records PKV_DEVERR_TIMEOUT (read by
+    device_error()) and its CTA exits without writing its rows."""
+    check(lib().pkv_set_wait_limit(int(clock_cycles)))
+
+
 _MODES = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL,
           "mixed": _lib.PKV_MODE_MIXED, "ragged": _lib.PKV_MODE_RAGGED}
 _KV_DTYPES = {"bf16": _lib.PKV_BF16, "e4m3": _lib.PKV_FP8_E4M3, "fp8": _lib.PKV_FP8_E4M3}

@@ -117,6 +117,8 @@ _SIGS = {
                                   C.c_int32, C.c_void_p]),
     "pkv_last_error": (C.c_char_p, []),
     "pkv_device_error": (C.c_int, [_i32p, C.c_int32, C.c_void_p]),
+    "pkv_set_wait_limit": (C.c_int, [C.c_int64]),
+    "pkv_test_hold_wait": (C.c_int, [C.c_int32]),
     "pkv_plan_info_get": (C.c_int, [C.c_void_p, C.POINTER(pkv_plan_info)]),
     "pkv_plan_work_items": (C.c_int, [C.c_void_p, _i32p, C.c_int64]),
     "pkv_block_table_to_csr": (C.c_int, [_i32p, C.c_int32, C.c_int32, _i32p, C.c_int32, _i32p, _i32p, C.c_int64, _i32p]),

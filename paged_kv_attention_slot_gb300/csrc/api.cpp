@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -54,6 +55,10 @@ constexpr int kPrefillTiles = 2;         // Q tiles per CTA (they share every K/
 constexpr int kPrefillKeyTile = 128;     // keys per K/V tile of the prefill kernel
 constexpr int kPrefillMinChunk = 256;    // never split a prefill key range below this many keys
 constexpr int kPrefillMaxSplits = 64;    // chunks per prefill item at most (the chunk grows instead)
+
+constexpr int64_t kDefaultWaitLimit = 4000000000LL;  // clock cycles per in-kernel wait (about 2 s)
+std::atomic<int64_t> g_wait_limit{kDefaultWaitLimit};
+std::atomic<int32_t> g_hold_wait{0};
 
 }  // namespace
 
@@ -494,7 +499,9 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   return PKV_OK;
 }
 
-int check_cache(const pkv_plan* P, const pkv_cache* c) {
+}  // namespace
+
+int pkv::check_cache(const pkv_plan* P, const pkv_cache* c) {
   if (!c) return fail(PKV_EINVAL, "cache is NULL");
   if (!c->k || !c->v) return fail(PKV_EINVAL, "cache k/v pointers are NULL");
   if (c->num_kv_heads != P->Hkv || c->head_dim != P->D || c->page_size != P->ps || c->dtype != P->kv_dtype)
@@ -515,6 +522,8 @@ int check_cache(const pkv_plan* P, const pkv_cache* c) {
   }
   return PKV_OK;
 }
+
+namespace {
 
 // Kernel parameters for the work items [first, first + count) of the plan.
 pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c, void* o, float* lse, int64_t first,
@@ -549,6 +558,8 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
   p.window_left = P->window_left;
   p.noncausal = P->causal ? 0 : 1;
   p.ragged_kv = P->ragged ? 1 : 0;
+  p.wait_limit_k = (int32_t)((g_wait_limit.load(std::memory_order_relaxed) + 1023) >> 10);
+  p.hold_wait = g_hold_wait.load(std::memory_order_relaxed);
   const float log2e = 1.4426950408889634f;
   p.scale_log2 = P->sm_scale * log2e * (c->dtype == PKV_FP8_E4M3 ? c->k_scale : 1.0f);
   p.out_scale = c->dtype == PKV_FP8_E4M3 ? c->v_scale : 1.0f;
@@ -564,7 +575,7 @@ int check_run(const pkv_plan* P, int mode, const void* q, const pkv_cache* c, vo
     return fail(PKV_EINVAL, mode == PKV_MODE_DECODE    ? "decode_run needs a PKV_MODE_DECODE or PKV_MODE_MIXED plan"
                             : mode == PKV_MODE_RAGGED ? "ragged_run needs a PKV_MODE_RAGGED plan"
                                                       : "prefill_run needs a PKV_MODE_PREFILL or PKV_MODE_MIXED plan");
-  int st = check_cache(P, c);
+  int st = pkv::check_cache(P, c);
   if (st != PKV_OK) return st;
   if (P->total_tokens > 0 && (!q || !o)) return fail(PKV_EINVAL, "q and o must be non-NULL");
   if (((uintptr_t)q | (uintptr_t)o) & 15) return fail(PKV_EINVAL, "q and o must be 16-byte aligned");
@@ -835,6 +846,17 @@ int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const 
   if (((uintptr_t)o_a | (uintptr_t)o_b | (uintptr_t)o) & 15) return fail(PKV_EINVAL, "o_a, o_b and o must be 16-byte aligned");
   PKV_CUDA(pkv::launch_merge_state(o_a, lse_a, o_b, lse_b, o, lse, num_states, head_dim, (cudaStream_t)stream),
            "merge launch");
+  return PKV_OK;
+}
+
+int pkv_set_wait_limit(int64_t clock_cycles) {
+  if (clock_cycles > ((int64_t)INT32_MAX << 10)) return fail(PKV_EINVAL, "clock_cycles is too large");
+  g_wait_limit.store(clock_cycles <= 0 ? kDefaultWaitLimit : clock_cycles, std::memory_order_relaxed);
+  return PKV_OK;
+}
+
+int pkv_test_hold_wait(int32_t on) {
+  g_hold_wait.store(on ? 1 : 0, std::memory_order_relaxed);
   return PKV_OK;
 }
 

@@ -143,11 +143,42 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
         qb[ks][nb][1] = valid ? *reinterpret_cast<const uint32_t*>(qr + ks * 16 + 8 + 2 * t) : 0u;
       } else {
         // permuted order: logical k {2t, 2t+1} <- dims 16ks+4t+{0,1}; {2t+8, 2t+9} <- 16ks+4t+{2,3}
+        // (raw bf16 pairs here; widened to f16 below)
         const uint2 x = valid ? *reinterpret_cast<const uint2*>(qr + ks * 16 + 4 * t) : make_uint2(0, 0);
-        qb[ks][nb][0] = pack_f16(__uint_as_float(x.x << 16), __uint_as_float(x.x & 0xffff0000u));
-        qb[ks][nb][1] = pack_f16(__uint_as_float(x.y << 16), __uint_as_float(x.y & 0xffff0000u));
+        qb[ks][nb][0] = x.x;
+        qb[ks][nb][1] = x.y;
       }
     }
+  }
+  // FP8 KV runs the products in f16, whose largest finite value is 65504: a larger |q| would become
+  // inf.  The CTA's Q rows are scaled by 2^-e, with e the smallest power that brings max |q| below
+  // 2^15, and the score scale is multiplied by 2^e.  The scaling is exact (a bf16 value inside the f16
+  // normal range is an f16 value), and e = 0 whenever max |q| < 2^15.
+  float sc = p.scale_log2;
+  if constexpr (FP8) {
+    uint32_t amax = 0;  // largest |q| as bf16 magnitude bits (monotonic in the value)
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t r = qb[ks][nb][h];
+          amax = max(amax, max(r & 0x7fffu, (r >> 16) & 0x7fffu));
+        }
+    amax = __reduce_max_sync(0xffffffffu, amax);  // every warp holds the CTA's whole Q
+    const int e = max(0, (int)(amax >> 7) - 127 - 14);  // bf16 exponent field -> floor(log2 max |q|)
+    const float down = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 114: a normal float)
+    sc *= __uint_as_float((uint32_t)(127 + e) << 23);              // 2^e
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t r = qb[ks][nb][h];
+          qb[ks][nb][h] = pack_f16(__uint_as_float(r << 16) * down, __uint_as_float(r & 0xffff0000u) * down);
+        }
   }
 
   // ---- per-warp cp.async ring ----
@@ -321,10 +352,10 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     uint32_t pb[NB][2];
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
-      float x0 = s[nb][0] * p.scale_log2;  // key g,     head 2t
-      float x1 = s[nb][1] * p.scale_log2;  // key g,     head 2t+1
-      float x2 = s[nb][2] * p.scale_log2;  // key g + 8, head 2t
-      float x3 = s[nb][3] * p.scale_log2;  // key g + 8, head 2t+1
+      float x0 = s[nb][0] * sc;  // key g,     head 2t
+      float x1 = s[nb][1] * sc;  // key g,     head 2t+1
+      float x2 = s[nb][2] * sc;  // key g + 8, head 2t
+      float x3 = s[nb][3] * sc;  // key g + 8, head 2t+1
       if (!full) {
         const bool lo_ok = key0 + g < w.kv_end, hi_ok = key0 + g + 8 < w.kv_end;
         x0 = lo_ok ? x0 : -INFINITY;

@@ -1,12 +1,13 @@
 // Decode for callers that cannot allocate device memory.
 //
 // Some hosts of this library cannot call cudaMalloc at all: code running inside another
-// framework's memory pool that forbids raw allocations, callers that must not allocate while a
-// CUDA graph is being captured, or embedded runtimes that are handed a fixed budget of device
-// memory up front.  For them, pkv_attn_decode_run_noalloc keeps everything the decode needs
-// besides its inputs and outputs -- the plan's work list, the per-request facts, the page list and
-// the split-KV partial outputs -- in one file-scope __device__ array of kNoAllocScratchBytes, and
-// runs the same decode kernel (with its split-KV merge) as pkv_attn_decode_run on it.
+// framework's memory pool that forbids raw allocations (an allocation behind the pool's back
+// breaks its accounting or its out-of-memory handling), or embedded runtimes that are handed a
+// fixed budget of device memory up front and must not grow past it.  For them,
+// pkv_attn_decode_run_noalloc keeps everything the decode needs besides its inputs and outputs --
+// the plan's work list, the per-request facts, the page list and the split-KV partial outputs -- in
+// one file-scope __device__ array of kNoAllocScratchBytes, and runs the same decode kernel (with
+// its split-KV merge) as pkv_attn_decode_run on it.
 //
 // The array exists once per device that loads the library and stays allocated until the process
 // exits.  Every call shares it and it keeps the last call's contents; nothing in it has to start at
@@ -14,11 +15,12 @@
 // partial slot a call reads was written earlier in the same call).  Two calls whose
 // work overlaps on the GPU (different streams, or different host threads without ordering) race
 // on the array.  The first call on a device looks up the array's device address; that first call
-// should be made before any stream capture begins.
+// should be made before any stream capture begins.  Each call copies the plan's metadata from the
+// plan's host arrays with ordinary (pageable) host-to-device copies.
 
 #include <cuda_runtime.h>
 
-#include <cmath>
+#include <atomic>
 #include <cstring>
 #include <string>
 
@@ -35,7 +37,9 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 namespace {
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+// Device address of the scratch array per device, filled by the first call on that device.  Two
+// host threads making that first call at once both look it up and store the same value.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 int noalloc_fail(int code, const std::string& msg) { return pkv::set_last_error(code, msg.c_str()); }
 
@@ -45,13 +49,13 @@ cudaError_t scratch_address(void** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
+  void* ptr = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = ptr;
+    g_scratch_addr[dev].store(ptr, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = ptr;
   return cudaSuccess;
 }
 
@@ -68,19 +72,11 @@ extern "C" int pkv_attn_decode_run_noalloc(const pkv_plan* plan, const void* q, 
     return noalloc_fail(PKV_EWORKSPACE, "the plan needs " + std::to_string(plan->need_bytes) +
                                             " bytes of scratch; the no-allocation path has " +
                                             std::to_string(kNoAllocScratchBytes));
-  if (!cache || !cache->k || !cache->v) return noalloc_fail(PKV_EINVAL, "cache is NULL");
-  if (cache->num_kv_heads != plan->Hkv || cache->head_dim != plan->D || cache->page_size != plan->ps ||
-      cache->dtype != plan->kv_dtype)
-    return noalloc_fail(PKV_EINVAL, "cache geometry (kv heads, head_dim, page_size, dtype) does not match the plan");
-  if (cache->num_pages <= plan->max_page_id) return noalloc_fail(PKV_EINVAL, "the plan references pages beyond the pool");
-  if (cache->dtype == PKV_FP8_E4M3 &&
-      (!(cache->k_scale > 0.f) || !(cache->v_scale > 0.f) || !std::isfinite(cache->k_scale) ||
-       !std::isfinite(cache->v_scale)))
-    return noalloc_fail(PKV_EINVAL, "FP8 cache scales must be finite and > 0");
+  // the same cache checks as every other run entry point (geometry against the plan, page range,
+  // alignment, positive strides, FP8 scales)
+  const int st = check_cache(plan, cache);
+  if (st != PKV_OK) return st;
   const int64_t esz = cache->dtype == PKV_FP8_E4M3 ? 1 : 2;
-  if (((uintptr_t)cache->k | (uintptr_t)cache->v) & 15 ||
-      (cache->stride_page * esz) % 16 || (cache->stride_token * esz) % 16 || (cache->stride_head * esz) % 16)
-    return noalloc_fail(PKV_EINVAL, "cache pointers and strides must be 16-byte aligned");
   if (plan->total_tokens > 0 && (!q || !o)) return noalloc_fail(PKV_EINVAL, "q and o must be non-NULL");
   if (((uintptr_t)q | (uintptr_t)o) & 15) return noalloc_fail(PKV_EINVAL, "q and o must be 16-byte aligned");
   if (plan->work.empty()) return PKV_OK;

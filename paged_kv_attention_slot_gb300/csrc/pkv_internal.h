@@ -92,6 +92,9 @@ struct RunParams {
   int32_t noncausal;   // prefill: 1 = every query sees all of its request's keys (0 = causal)
   int32_t ragged_kv;   // prefill: 1 = key j of request i is row page_base + j of the pools (no page table)
   int32_t merge_into;  // prefill: 1 = merge this pass's state into the state held in (o, lse) (LSE weights)
+  int32_t wait_limit_k;  // prefill: bound on each in-kernel wait, in units of 1024 SM clock cycles
+  int32_t hold_wait;     // prefill: 1 = the MMA thread first waits on a barrier nothing arrives at (the
+                         // wait runs out and the CTA takes its timeout path; a test of that path)
   float scale_log2;    // sm_scale * log2(e) (* k_scale for FP8 KV)
   float out_scale;     // 1, or v_scale for FP8 KV
   int64_t num_work;
@@ -116,6 +119,10 @@ cudaError_t read_device_error(int32_t* code, int reset, cudaStream_t s);
 
 // record `msg` as this thread's pkv_last_error() text and return `code`
 int set_last_error(int code, const char* msg);
+
+// The run-time checks of a KV cache against a plan (geometry, page range, alignment, positive
+// strides, FP8 scales); PKV_OK or an error status with its message set.
+int check_cache(const pkv_plan* P, const pkv_cache* c);
 
 }  // namespace pkv
 

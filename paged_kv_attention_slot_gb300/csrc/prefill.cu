@@ -34,8 +34,8 @@
 //    by more than 2^8; exact because numerator and denominator share it), and O is rescaled in TMEM
 //    only then, before the first half is signalled.  Epilogue: O / l to bf16 rows and the LSE, or an
 //    fp32 partial of a split item.
-// Registers are rebalanced with setmaxnreg: the two softmax warpgroups take 176 per thread, the
-// producer and MMA warpgroups keep 80.  Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its own
+// Registers are rebalanced with setmaxnreg: the two softmax warpgroups take 184 per thread, the
+// producer and MMA warpgroups keep 72.  Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its own
 // copies and MMAs, frees its TMEM and exits.
 
 #include <cuda.h>
@@ -62,7 +62,7 @@ constexpr int OFF_QB = OFF_QA + TILE_B;
 constexpr int OFF_K = OFF_QB + TILE_B;
 constexpr int OFF_V = OFF_K + STAGES * TILE_B;
 constexpr int OFF_BAR = OFF_V + STAGES * TILE_B;
-constexpr int NUM_BARS = 18;
+constexpr int NUM_BARS = 19;
 constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
 constexpr int SMEM_USED = OFF_ABORT + 8;
@@ -73,7 +73,8 @@ enum {
   B_PF = 11,  // [2]: all of P_X(j) stored in TMEM by the 4 softmax warps of tile X
   B_OD = 13,  // [2]: the last PV_X complete
   B_FIN = 15,
-  B_PH = 16   // [2]: the first half (keys 0-63) of P_X(j) stored by the 4 softmax warps of tile X
+  B_PH = 16,  // [2]: the first half (keys 0-63) of P_X(j) stored by the 4 softmax warps of tile X
+  B_HOLD = 18  // nothing arrives here: the held wait of a timeout-path test
 };
 constexpr uint32_t TMEM_COLS = 512;  // S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384), O_B [384,512)
 constexpr uint32_t TMEM_O = 256;
@@ -89,7 +90,10 @@ constexpr uint32_t SOFTMAX_REGS = 184;
 constexpr uint32_t OTHER_REGS = 72;
 constexpr int K_PRODUCER_THREADS = 32 * K_WARPS;
 constexpr int V_PRODUCER_THREADS = 32 * V_WARPS;
-constexpr long long WAIT_LIMIT = 4000000000LL;  // clock cycles (about 2 s)
+// The waits of the pipeline give up after the run's limit (RunParams::wait_limit_k x 1024 clock
+// cycles, about 2 s by default); the waits of the timeout path itself, for copies and MMAs already
+// in flight, use DRAIN_LIMIT whatever the run's limit.
+constexpr long long DRAIN_LIMIT = 500000000LL;  // clock cycles (about 0.25 s)
 constexpr float RESCALE_THRESHOLD = 8.0f;      // log2 units
 }  // namespace pf
 
@@ -139,6 +143,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const int T = ROWS / G;              // tokens per Q tile
   const bool two = w.q_rows > T;       // does tile B hold any token?
   const int nkt = (w.kv_end - w.kv_begin + KT - 1) / KT;
+  const long long wait_limit = (long long)p.wait_limit_k << 10;
   (void)tk;
   (void)tv;
 
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       tc::mbar_init(BAR(B_OD + x), 1);
     }
     tc::mbar_init(BAR(B_FIN), 1);
+    tc::mbar_init(BAR(B_HOLD), 1);
     tc::mbar_fence_init();
   }
   if (warp == MMA_WARP) {
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         next_a = slot_idx(j + 1, lane);
         next_b = slot_idx(j + 1, 32 + lane);
       }
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, WAIT_LIMIT));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, wait_limit));
       if (!ok) break;
       const uint32_t dst0 = s_base + st * TILE_B + half * HALF_B;
 #pragma unroll 4
@@ -268,6 +274,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     if (!ok) {
       *abort_flag = 1;
       if (lane == 0) record_error(err, PKV_DEVERR_TIMEOUT);
+    }
+    // the Q tiles must have landed before the CTA exits, also when the MMA thread gave up before
+    // waiting for them (returns at once otherwise)
+    if (warp == PRODUCER_WARP0 && lane == 0) {
+      volatile int never = 0;
+      tc::mbar_wait(BAR(B_Q), 0, &never, DRAIN_LIMIT);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------------ MMA issuer
@@ -297,9 +309,11 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         }
       };
       auto wait = [&](uint32_t bar, uint32_t parity) {
-        return tc::mbar_wait(bar, parity, abort_flag, WAIT_LIMIT);
+        return tc::mbar_wait(bar, parity, abort_flag, wait_limit);
       };
-      bool ok = wait(BAR(B_Q), 0) && wait(BAR(B_KF), 0);
+      // a test of the timeout path holds the thread on a barrier nothing arrives at
+      bool ok = !p.hold_wait || wait(BAR(B_HOLD), 0);
+      ok = ok && wait(BAR(B_Q), 0) && wait(BAR(B_KF), 0);
       if (ok) {
         tc::fence_proxy_async_smem();
         tc::fence_after_sync();
@@ -350,7 +364,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         // every MMA issued so far must be complete before the TMEM is freed
         tc::commit(BAR(B_FIN));
         volatile int never = 0;
-        tc::mbar_wait(BAR(B_FIN), 0, &never, WAIT_LIMIT / 8);
+        tc::mbar_wait(BAR(B_FIN), 0, &never, DRAIN_LIMIT);
       }
     }
     __syncwarp();
@@ -375,7 +389,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkt; ++j) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_SF + x), j & 1, abort_flag, WAIT_LIMIT));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_SF + x), j & 1, abort_flag, wait_limit));
       if (!ok) break;
       tc::fence_after_sync();
       const int k0 = w.kv_begin + j * KT;
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       f2unpack(sum2[1], sa[2], sa[3]);
       l += (sa[0] + sa[1]) + (sa[2] + sa[3]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD + x), 0, abort_flag, WAIT_LIMIT));
+    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(BAR(B_OD + x), 0, abort_flag, wait_limit));
     if (ok && w.out_slot >= 0) {
       // one key chunk of a split item: normalised fp32 partial + log2-sum-exp, merged afterwards.
       // O goes out as [32 four-column groups][256 rows] float4, so each store is coalesced.

@@ -103,6 +103,37 @@ def test_run_on_host_only_plan_fails_loudly(pk):
     assert "host-only" in pk._lib.lib().pkv_last_error().decode()
 
 
+@pytest.mark.parametrize("strides", [(0, 256, 128), (4096, 0, 128), (4096, 256, 0), (-4096, 256, 128),
+                                     (4096, -256, 128), (4096, 256, -128)])
+def test_noalloc_decode_rejects_non_positive_strides_before_any_launch(pk, strides):
+    # the no-allocation decode runs the same cache checks as pkv_attn_decode_run: a zero or negative
+    # stride (which passes the 16-byte test) would make the kernel gather outside the pool
+    import ctypes as C
+
+    p = _plan(pk)
+    cache = pk._lib.pkv_cache(16, 16, 4, 16, 2, 128, 0, *strides, 1.0, 1.0)
+    st = pk._lib.lib().pkv_attn_decode_run_noalloc(p._h, 16, C.byref(cache), 16, None, None)
+    assert st == pk._lib.PKV_EINVAL
+    assert "positive" in pk._lib.lib().pkv_last_error().decode()
+
+
+def test_noalloc_decode_checks_the_cache_against_the_plan(pk):
+    import ctypes as C
+
+    p = _plan(pk)
+    L = pk._lib.lib()
+    for args in [(16, 16, 4, 16, 4, 128, 0, 4096, 256, 128, 1.0, 1.0),   # kv heads differ from the plan
+                 (16, 16, 3, 16, 2, 128, 0, 4096, 256, 128, 1.0, 1.0),   # page 3 is beyond a 3-page pool
+                 (24, 16, 4, 16, 2, 128, 0, 4096, 256, 128, 1.0, 1.0),   # misaligned pool pointer
+                 (16, 16, 4, 16, 2, 128, 0, 4100, 256, 128, 1.0, 1.0)]:  # stride not a multiple of 16 B
+        cache = pk._lib.pkv_cache(*args)
+        assert L.pkv_attn_decode_run_noalloc(p._h, 16, C.byref(cache), 16, None, None) == pk._lib.PKV_EINVAL
+    fp8 = _plan(pk, kv_dtype="e4m3")
+    cache = pk._lib.pkv_cache(16, 16, 4, 16, 2, 128, 1, 4096, 256, 128, 0.0, 1.0)  # FP8 scale 0
+    assert L.pkv_attn_decode_run_noalloc(fp8._h, 16, C.byref(cache), 16, None, None) == pk._lib.PKV_EINVAL
+    assert "scale" in L.pkv_last_error().decode()
+
+
 def _check_decode_cover(b, items, window=-1, group=None):
     """Every (request, kv head, head group) has its whole visible key range [lo, L) planned exactly once:
     either one CTA reading it alone (no partial slot), or several CTAs that share it (they claim its

@@ -118,6 +118,31 @@ def _decode_case(b, **plan_kw):
     return G.compare(out, lse, ro, rl, max_abs=tol), plan
 
 
+def test_decode_fp8_query_beyond_the_f16_range():
+    # FP8 KV runs the decode products in f16, whose largest finite value is 65504; query rows with
+    # |q| up to ~1.2e5 are scaled into range by a power of two inside the kernel (exact for bf16
+    # values), so the output stays within the FP8 tolerance of the oracle instead of turning NaN.
+    # The heads that share a CTA with a large one (same KV head) are checked too.
+    b = W.make_batch([700, 20, 5000, 129, 3000], [1] * 5, 16, 32, 8, 128, seed=91, kv_dtype="e4m3")
+    q = b.q.float()
+    q[0, 0:4] *= 3e4                 # one whole KV-head group of request 0: |q| up to ~1.2e5
+    q[2, 5, 17] = 1.0e5              # a single element of request 2 (its KV head's other heads stay N(0,1))
+    q[2, 6, 100] = -7.0e4
+    q[3, :] *= 2e4                   # every head of request 3: |q| up to ~8e4
+    b.q = q.bfloat16()
+    assert float(b.q.float().abs().max()) > 65504
+    g = G.GpuBatch(b)
+    g.store()
+    out, lse = g.run(g.plan())
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt)
+    # an fp32 score of magnitude ~1e5 carries ~1e-2 of rounding: the LSE bound grows with |lse|
+    G.compare(out, lse, ro, rl, max_abs=G.FP8_MAX_ABS, lse_rel=1e-6)
+    # the same batch with the split-KV merge forced
+    out, lse = g.run(g.plan(num_sms=4096))
+    G.compare(out, lse, ro, rl, max_abs=G.FP8_MAX_ABS, lse_rel=1e-6)
+
+
 def test_decode_tiny_workload_all_elements():
     stats, plan = _decode_case(W.workload(1))
     assert plan.info()["num_merge"] == 0

@@ -71,14 +71,22 @@ def test_prefill_custom_scale_large_scores():
 
 
 def test_prefill_full_size_prefix_extend_sampled():
+    # the benchmark's launch (all 1448 CTAs of the prefix-extend workload): every token row and head
+    # of its longest and its shortest request, plus sampled rows of every other request
     b = W.workload(3)
     rng = np.random.default_rng(3)
     rows = []
+    n = np.diff(b.qo_indptr)
+    whole = {int(np.argmax(n)), int(np.argmin(n))}
     for i in range(b.batch_size):
         q0, q1 = int(b.qo_indptr[i]), int(b.qo_indptr[i + 1])
-        rows += [q0, q1 - 1] + rng.integers(q0, q1, size=3).tolist()
+        if i in whole:
+            rows += list(range(q0, q1))
+        else:
+            rows += [q0, q1 - 1] + rng.integers(q0, q1, size=3).tolist()
     stats, plan = _case(b, rows=sorted(set(rows)))
     assert plan.info()["num_work"] > 1000
+    assert len(rows) > int(n.max()) + int(n.min())
 
 
 # ---- split-KV prefill: few query items over long key ranges --------------------------------------

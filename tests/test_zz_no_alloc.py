@@ -1,8 +1,8 @@
 """pkv_attn_decode_run_noalloc: decode for callers that cannot allocate device memory.
 
-Such callers (a host framework whose memory pool forbids raw cudaMalloc, code in the middle of
-building a CUDA graph, an embedded runtime with a fixed device-memory budget) cannot provide the
-plan workspace; this entry point keeps the plan metadata and the split-KV partials in the
+Such callers (a host framework whose memory pool forbids raw cudaMalloc, because an allocation
+behind the pool's back breaks its accounting; an embedded runtime with a fixed device-memory budget)
+cannot provide the plan workspace; this entry point keeps the plan metadata and the split-KV partials in the
 library's own static device array instead.  The test calls it through the C ABI, twice in a row on
 different batches (and once more on the first), and checks each result against the ordinary
 workspace-based pkv_attn_decode_run on the same plan arguments.
