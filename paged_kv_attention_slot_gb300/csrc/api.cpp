@@ -55,6 +55,8 @@ constexpr int kPrefillTiles = 2;         // Q tiles per CTA (they share every K/
 constexpr int kPrefillKeyTile = 128;     // keys per K/V tile of the prefill kernel
 constexpr int kPrefillMinChunk = 256;    // never split a prefill key range below this many keys
 constexpr int kPrefillMaxSplits = 64;    // chunks per prefill item at most (the chunk grows instead)
+constexpr bool kPrefillGroupOrder = true;  // prefill CTAs grouped by (request, KV head) for L2 reuse
+constexpr int kPrefillTailNum = 10, kPrefillTailDen = 100;  // share of the work ordered longest first at the end
 
 constexpr int64_t kDefaultWaitLimit = 4000000000LL;  // clock cycles per in-kernel wait (about 2 s)
 std::atomic<int64_t> g_wait_limit{kDefaultWaitLimit};
@@ -127,6 +129,49 @@ void order_longest_first(std::vector<WorkItem>& all, size_t begin, size_t end) {
   WorkItem* dst = tmp.data();
   for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - (k[i] >> shift)]++] = w[i];
   std::memcpy(w, dst, n * sizeof(WorkItem));
+}
+
+// Group-major order of the prefill items on top of the longest-first order: the (request, KV head)
+// groups by total work, largest first, and inside a group its items still longest first (a stable
+// counting sort on the group's rank).  The CTAs resident at any moment then come from a few groups,
+// so the K/V rows they gather stay in L2 between the query tiles that read them.
+void order_by_group(std::vector<WorkItem>& all, size_t begin, size_t end, int32_t num_kv_heads) {
+  const size_t n = end - begin;
+  if (n < 2) return;
+  WorkItem* w = all.data() + begin;
+  int32_t max_req = 0;
+  for (size_t i = 0; i < n; ++i) max_req = std::max(max_req, w[i].req);
+  const size_t ng = (size_t)(max_req + 1) * (size_t)num_kv_heads;
+  thread_local std::vector<int64_t> total;
+  thread_local std::vector<int32_t> rank, order;
+  total.assign(ng, 0);
+  for (size_t i = 0; i < n; ++i) total[(size_t)w[i].req * num_kv_heads + w[i].kv_head] += item_share(w[i]);
+  order.resize(ng);
+  for (size_t g = 0; g < ng; ++g) order[g] = (int32_t)g;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return total[a] > total[b]; });
+  rank.resize(ng);
+  for (size_t r = 0; r < ng; ++r) rank[order[r]] = (int32_t)r;
+  thread_local std::vector<uint32_t> count;
+  thread_local std::vector<WorkItem> tmp;
+  count.assign(ng + 1, 0u);
+  tmp.resize(n);
+  for (size_t i = 0; i < n; ++i) ++count[rank[(size_t)w[i].req * num_kv_heads + w[i].kv_head] + 1];
+  for (size_t g = 0; g < ng; ++g) count[g + 1] += count[g];
+  for (size_t i = 0; i < n; ++i) tmp[count[rank[(size_t)w[i].req * num_kv_heads + w[i].kv_head]]++] = w[i];
+  std::memcpy(w, tmp.data(), n * sizeof(WorkItem));
+  // the last part of the work goes longest first again, so that no long item starts near the end
+  int64_t all_work = 0;
+  for (size_t g = 0; g < ng; ++g) all_work += total[g];
+  int64_t acc = 0;
+  size_t cut = n;
+  for (size_t i = 0; i < n; ++i) {
+    acc += item_share(w[i]);
+    if (acc * kPrefillTailDen > all_work * (kPrefillTailDen - kPrefillTailNum)) {
+      cut = i + 1;
+      break;
+    }
+  }
+  if (kPrefillTailNum > 0) order_longest_first(all, begin + cut, end);
 }
 
 // Validate the arguments and build the work list into P (no device work).
@@ -469,6 +514,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   // longest first: the block scheduler hands out CTAs roughly in launch order
   order_longest_first(P->work, 0, (size_t)P->num_decode_work);
   order_longest_first(P->work, (size_t)P->num_decode_work, P->work.size());
+  if (kPrefillGroupOrder) order_by_group(P->work, (size_t)P->num_decode_work, P->work.size(), a->num_kv_heads);
   if ((int64_t)P->work.size() > INT32_MAX) return fail(PKV_EUNSUPPORTED, "too many CTAs");
 
   // workspace layout: [work][merge][req][kv_indices] | [partial lse][partial o]

@@ -605,3 +605,30 @@ def test_host_helpers_match_the_oracle_on_random_tables(pk, seed):
     if seq.max() > 0:
         tt = rng.integers(0, 1 << 20, (B, int(seq.max()) + int(rng.integers(0, 4)))).astype(np.int32)
         assert np.array_equal(pk.token_table_to_page_table(tt, seq, ps), M.page_table_from_token_table(tt, seq, ps))
+
+
+def test_prefill_order_groups_requests_and_kv_heads_with_a_longest_first_tail(pk):
+    # prefill CTAs come group by group ((request, KV head), largest total first, each group longest
+    # first) so that the CTAs resident together share K/V rows in L2; the last ~10 % of the work is
+    # longest first again, so no long item starts near the end.  Every key is still planned once.
+    import workloads as W
+
+    b = W.workload(3)
+    p = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=32,
+                       num_kv_heads=8, head_dim=128, page_size=1, mode="prefill", num_sms=152, host_only=True)
+    it = p.work_items()  # req, kv_head, head_group, kv_begin, kv_end, q_row, out_slot, q_rows
+    share = (it[:, 4] - it[:, 3]).astype(np.int64)
+    total = share.sum()
+    cut = int(np.searchsorted(np.cumsum(share), 0.9 * total, side="right")) + 1
+    head, tail = it[:cut], share[cut:]
+    # the tail is longest first (up to the counting sort's bucket width)
+    assert np.all(np.diff(tail) <= share.max() // 64 + 1)
+    # the head is a sequence of contiguous groups, largest group total first, each longest first
+    groups = head[:, 0] * 8 + head[:, 1]
+    starts = np.flatnonzero(np.r_[True, groups[1:] != groups[:-1]])
+    assert len(starts) == len(np.unique(groups)), "a group is split in the head"
+    g_total = {g: share[(it[:, 0] * 8 + it[:, 1]) == g].sum() for g in np.unique(groups)}
+    seq = [g_total[groups[s0]] for s0 in starts]
+    assert all(x >= y for x, y in zip(seq, seq[1:]))
+    for s0, s1 in zip(starts, list(starts[1:]) + [cut]):
+        assert np.all(np.diff(share[s0:s1]) <= share.max() // 64 + 1)
