@@ -624,17 +624,30 @@ def next_rows_measure(device, peak_tflops, hbm):
         rag.run_ragged(st["q"], st["k_new"], st["v_new"], out=o1, lse=s1)
         pre.run(st["q"], st["cache"], out=o1, lse=s1, merge_into=True)
 
+    # one launch over both sources: prefix pages + the new tokens' contiguous rows, one online softmax
+    one = pk.Plan().plan(b.qo_indptr, pi, px.astype(np.int32), pl, page_size=ps, mode="paged_ragged", **kw)
+
+    def extend_one_pass():
+        one.run_paged_ragged(st["q"], st["cache"], st["k_new"], st["v_new"], out=o1)
+
     flops = 4.0 * b.head_dim * b.num_qo_heads * _visible_pairs(b.kv_len, b.q_len)
-    ms, mode = kernel_ms(extend_by_merge, reps=10, iters=5)
+    ms_one, mode = kernel_ms(extend_one_pass, reps=10, iters=5)
+    ms, _ = kernel_ms(extend_by_merge, reps=10, iters=5)
     ms_fused, _ = kernel_ms(extend_by_fused_merge, reps=10, iters=5)
+    tf = lambda t: flops / (t * 1e-3) / 1e12  # noqa: E731
     out["extend_by_merge"] = {
-        "workload": "prefix_extend (as the prefill line) computed as ragged + paged prefix + merge",
-        "launches": 3 + (1 if pre.info()["num_merge"] else 0),
-        "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
-        "frac": round(flops / (ms * 1e-3) / 1e12 / peak_tflops, 4), "timing": mode,
-        "plans": {"ragged_ctas": rag.info()["num_work"], "prefix_ctas": pre.info()["num_work"]},
-        "fused": {"launches": 2, "ms": round(ms_fused, 4), "tflops": round(flops / (ms_fused * 1e-3) / 1e12, 2),
-                  "frac": round(flops / (ms_fused * 1e-3) / 1e12 / peak_tflops, 4),
+        "workload": "prefix_extend (as the prefill line) with the new tokens' K/V as contiguous (ragged) rows "
+                    "and the cached prefix through the page table",
+        "launches": 1, "ms": round(ms_one, 4), "tflops": round(tf(ms_one), 2),
+        "frac": round(tf(ms_one) / peak_tflops, 4), "timing": mode,
+        "how": "one prefill launch over both sources (PKV_MODE_PAGED_RAGGED), one online softmax, no merge",
+        "plans": {"one_pass_ctas": one.info()["num_work"], "ragged_ctas": rag.info()["num_work"],
+                  "prefix_ctas": pre.info()["num_work"]},
+        "three_calls": {"launches": 3 + (1 if pre.info()["num_merge"] else 0), "ms": round(ms, 4),
+                        "tflops": round(tf(ms), 2), "frac": round(tf(ms) / peak_tflops, 4),
+                        "how": "ragged pass + paged prefix pass + LSE merge"},
+        "fused": {"launches": 2, "ms": round(ms_fused, 4), "tflops": round(tf(ms_fused), 2),
+                  "frac": round(tf(ms_fused) / peak_tflops, 4),
                   "how": "the paged prefix pass merges into the ragged pass's (o, lse) in its epilogue"}}
     del st, rag, pre, o1, o2, s1, s2
     torch.cuda.empty_cache()

@@ -63,10 +63,18 @@ typedef enum {
                          * of "vLLM 源码完全拆解（六）：Attention Backend", sections «为什么先把 Decode
                          * 移到前面» and «FlashInfer Builder 的结果»).  Requests may come in any order: every
                          * CTA carries its own token row, so no decode-first reordering is needed. */
-  PKV_MODE_RAGGED = 3   /* prefill / extend over CONTIGUOUS K/V tensors instead of the paged pool
+  PKV_MODE_RAGGED = 3,  /* prefill / extend over CONTIGUOUS K/V tensors instead of the paged pool
                          * (the ragged form of "SGLang 源码完全拆解(八)：Attention Backend", section
                          * «extend 的两种形态»): kv_indptr holds TOKEN offsets into k / v, kv_indices,
                          * last_page_len and page_size are ignored; run with pkv_attn_ragged_run. */
+  PKV_MODE_PAGED_RAGGED = 4 /* prefill / extend in one pass over TWO sources: kv_indptr, kv_indices and
+                         * last_page_len describe only each request's CACHED PREFIX in the paged
+                         * pool (no pages = no prefix), and the n_i new tokens' K/V are rows
+                         * qo_indptr[i].. of contiguous k_new / v_new tensors (the "ragged" segment).
+                         * Key j < prefix_i comes from the pool, key prefix_i + t from new row t, and
+                         * one online softmax covers both: the result of the paged + ragged + merge form
+                         * of "SGLang 源码完全拆解(八)：Attention Backend", section «extend 的两种形态»,
+                         * without the separate passes or the merge.  Run with pkv_attn_paged_ragged_run. */
 } pkv_mode;
 
 /* Device error codes a kernel may record (read with pkv_device_error). */
@@ -283,6 +291,20 @@ int pkv_attn_ragged_run(const pkv_plan* plan, const void* q, const void* k, cons
  * o may alias o_a or o_b and lse may alias lse_a or lse_b (in-place merge).  head_dim 64 or 128.
  * Arithmetic in float32, output rounded to bf16 once.
  */
+/*
+ * pkv_attn_paged_ragged_run: run a PKV_MODE_PAGED_RAGGED plan (a5 over two K/V sources).
+ *   q      device bf16 [total_tokens, Hq, D], row-contiguous.
+ *   cache  the paged pool holding every request's cached prefix (the plan's page table).
+ *   k_new, v_new  device bf16 [total_tokens, Hkv, D], row-contiguous, 16-byte aligned: row r is the K /
+ *          V of new token r (the same rows as q); they need not be in the pool (the KV write of this
+ *          step may come before or after this call, on the caller's stream order).
+ *   o, lse as pkv_attn_prefill_run.
+ * Token t of request i sits at position P = prefix_i + t and sees keys 0..P (causal, optional window)
+ * or every key (causal == 0).
+ */
+int pkv_attn_paged_ragged_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, const void* k_new,
+                              const void* v_new, void* o, float* lse, void* stream);
+
 int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
                     int64_t num_states, int32_t head_dim, void* stream);
 

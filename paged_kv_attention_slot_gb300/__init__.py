@@ -155,7 +155,7 @@ def set_wait_limit(clock_cycles: int = 0) -> None:
 
 
 _MODES = {"decode": _lib.PKV_MODE_DECODE, "prefill": _lib.PKV_MODE_PREFILL, "extend": _lib.PKV_MODE_PREFILL,
-          "mixed": _lib.PKV_MODE_MIXED, "ragged": _lib.PKV_MODE_RAGGED}
+          "mixed": _lib.PKV_MODE_MIXED, "ragged": _lib.PKV_MODE_RAGGED, "paged_ragged": _lib.PKV_MODE_PAGED_RAGGED}
 _KV_DTYPES = {"bf16": _lib.PKV_BF16, "e4m3": _lib.PKV_FP8_E4M3, "fp8": _lib.PKV_FP8_E4M3}
 
 
@@ -273,6 +273,25 @@ class Plan:
                                         lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
         return (out, lse) if (return_lse or lse is not None) else out
 
+    def run_paged_ragged(self, q: torch.Tensor, cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                         out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = False,
+                         stream=None):
+        """Attention of a "paged_ragged" plan in one pass: the page table holds each request's cached
+        prefix in `cache`; k_new, v_new are contiguous bf16 [total_tokens, num_kv_heads, head_dim] holding
+        the new tokens' K / V (row r = token r of q)."""
+        if self.mode != "paged_ragged":
+            raise ValueError("run_paged_ragged needs a plan made with mode='paged_ragged'")
+        for name, t in (("k_new", k_new), ("v_new", v_new)):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bf16 tensor")
+            if tuple(t.shape) != (self.total_tokens, self.num_kv_heads, self.head_dim):
+                raise ValueError(f"{name} must be [{self.total_tokens}, {self.num_kv_heads}, {self.head_dim}]")
+        out, lse = self._outputs(q, out, lse, return_lse)
+        check(lib().pkv_attn_paged_ragged_run(self._h, q.data_ptr(), C.byref(cache.struct), k_new.data_ptr(),
+                                              v_new.data_ptr(), out.data_ptr(),
+                                              lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
+        return (out, lse) if (return_lse or lse is not None) else out
+
     def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
             return_lse: bool = False, merge_into: bool = False, stream=None):
         """Attention for every planned token row; q is [total_tokens, num_qo_heads, head_dim] bf16.
@@ -281,6 +300,8 @@ class Plan:
         new tokens) and receive the merge of that state with this pass's (pkv_attn_prefill_run_merge)."""
         if self.mode == "ragged":
             raise ValueError("a ragged plan runs with run_ragged(q, k, v)")
+        if self.mode == "paged_ragged":
+            raise ValueError("a paged_ragged plan runs with run_paged_ragged(q, cache, k_new, v_new)")
         if merge_into:
             if self.mode not in ("prefill", "extend") or out is None or lse is None:
                 raise ValueError("merge_into needs a prefill plan and the held state in out and lse")
@@ -337,6 +358,25 @@ class CascadePlan:
         self.suffix.plan(qo, kv_indptr, kv_indices, last_page_len, mode=mode, **kw)
         self.total_tokens = T
         return self
+
+    def run_paged_ragged(self, q: torch.Tensor, cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                         out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = False,
+                         stream=None):
+        """Attention of a "paged_ragged" plan in one pass: the page table holds each request's cached
+        prefix in `cache`; k_new, v_new are contiguous bf16 [total_tokens, num_kv_heads, head_dim] holding
+        the new tokens' K / V (row r = token r of q)."""
+        if self.mode != "paged_ragged":
+            raise ValueError("run_paged_ragged needs a plan made with mode='paged_ragged'")
+        for name, t in (("k_new", k_new), ("v_new", v_new)):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bf16 tensor")
+            if tuple(t.shape) != (self.total_tokens, self.num_kv_heads, self.head_dim):
+                raise ValueError(f"{name} must be [{self.total_tokens}, {self.num_kv_heads}, {self.head_dim}]")
+        out, lse = self._outputs(q, out, lse, return_lse)
+        check(lib().pkv_attn_paged_ragged_run(self._h, q.data_ptr(), C.byref(cache.struct), k_new.data_ptr(),
+                                              v_new.data_ptr(), out.data_ptr(),
+                                              lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
+        return (out, lse) if (return_lse or lse is not None) else out
 
     def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
             return_lse: bool = False, stream=None):

@@ -26,6 +26,7 @@ PKV_MODE_DECODE = 0
 PKV_MODE_PREFILL = 1
 PKV_MODE_MIXED = 2
 PKV_MODE_RAGGED = 3
+PKV_MODE_PAGED_RAGGED = 4
 
 STATUS_NAMES = {0: "PKV_OK", -1: "PKV_EINVAL", -2: "PKV_EUNSUPPORTED", -3: "PKV_EWORKSPACE", -4: "PKV_ECUDA",
                 -5: "PKV_EDEVICE"}
@@ -113,6 +114,8 @@ _SIGS = {
     "pkv_attn_prefill_run": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_attn_prefill_run_merge": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_attn_ragged_run": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
+    "pkv_attn_paged_ragged_run": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p,
+                                            C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_merge_state": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
                                   C.c_int32, C.c_void_p]),
     "pkv_last_error": (C.c_char_p, []),

@@ -180,9 +180,10 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   const int32_t B = a->batch_size;
   if (B < 0) return fail(PKV_EINVAL, "batch_size < 0");
   if (a->mode != PKV_MODE_DECODE && a->mode != PKV_MODE_PREFILL && a->mode != PKV_MODE_MIXED &&
-      a->mode != PKV_MODE_RAGGED)
+      a->mode != PKV_MODE_RAGGED && a->mode != PKV_MODE_PAGED_RAGGED)
     return fail(PKV_EINVAL, "unknown mode");
   const bool ragged = a->mode == PKV_MODE_RAGGED;  // K/V rows of contiguous tensors, no page table
+  const bool two_src = a->mode == PKV_MODE_PAGED_RAGGED;  // pages = prefix, new rows contiguous
   if (B > 0 && (!a->qo_indptr || !a->kv_indptr || (!ragged && !a->last_page_len)))
     return fail(PKV_EINVAL, ragged ? "qo_indptr and kv_indptr must be non-NULL"
                                    : "qo_indptr, kv_indptr and last_page_len must be non-NULL");
@@ -194,8 +195,8 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   if (a->causal != 0 && a->causal != 1) return fail(PKV_EINVAL, "causal must be 0 or 1");
   if (a->window_left < -1) return fail(PKV_EINVAL, "window_left must be -1 or >= 0");
   const bool causal = a->causal == 1;
-  if (!causal && a->mode != PKV_MODE_PREFILL && !ragged)
-    return fail(PKV_EINVAL, "causal == 0 needs a PKV_MODE_PREFILL or PKV_MODE_RAGGED plan");
+  if (!causal && a->mode != PKV_MODE_PREFILL && !ragged && !two_src)
+    return fail(PKV_EINVAL, "causal == 0 needs a PKV_MODE_PREFILL, PKV_MODE_RAGGED or PKV_MODE_PAGED_RAGGED plan");
   if (!causal && a->window_left >= 0) return fail(PKV_EINVAL, "a sliding window needs causal == 1");
   if (!(std::isfinite(a->sm_scale))) return fail(PKV_EINVAL, "sm_scale is not finite");
   if (a->q_dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "q_dtype must be PKV_BF16");
@@ -205,7 +206,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   if (a->max_splits < 0) return fail(PKV_EINVAL, "max_splits < 0");
   const int32_t G = a->num_qo_heads / a->num_kv_heads;
   // requests with more than one new token go to the prefill kernel (all of them in prefill mode)
-  bool any_extend = a->mode == PKV_MODE_PREFILL || ragged;
+  bool any_extend = a->mode == PKV_MODE_PREFILL || ragged || two_src;
   if (a->mode == PKV_MODE_MIXED)
     for (int32_t i = 0; i < B && !any_extend; ++i) any_extend = a->qo_indptr[i + 1] - a->qo_indptr[i] > 1;
   if (any_extend) {
@@ -241,6 +242,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
         return fail(PKV_EINVAL, "last_page_len must be in [1, page_size] (request " + std::to_string(i) + ")");
       L = (np - 1) * (int64_t)a->page_size + last;
     }
+    if (two_src) L += n;  // the pages hold the prefix; the new tokens follow it
     if (L > INT32_MAX) return fail(PKV_EUNSUPPORTED, "KV length exceeds 2^31-1");
     if (causal && L < n)
       return fail(PKV_EINVAL, "kv_len < q_len (request " + std::to_string(i) + "): seq_len - query_len must be the cached context");
@@ -293,6 +295,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
   P->ps = ragged ? 1 : a->page_size;
   P->causal = causal;
   P->ragged = ragged;
+  P->paged_ragged = two_src;
   P->window_left = a->window_left;
   P->kv_dtype = a->kv_dtype;
   P->q_dtype = a->q_dtype;
@@ -310,7 +313,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
 
   // decode rows: every request in decode mode, the one-token requests in mixed mode
   const bool plan_decode = a->mode == PKV_MODE_DECODE || a->mode == PKV_MODE_MIXED;
-  const bool plan_prefill = a->mode == PKV_MODE_PREFILL || a->mode == PKV_MODE_MIXED || ragged;
+  const bool plan_prefill = a->mode == PKV_MODE_PREFILL || a->mode == PKV_MODE_MIXED || ragged || two_src;
   if (plan_decode) {
     const int32_t groups = (G + pkv::kDecodeRows - 1) / pkv::kDecodeRows;
     struct Unit { int32_t req, lo, hi; };
@@ -604,6 +607,8 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
   p.window_left = P->window_left;
   p.noncausal = P->causal ? 0 : 1;
   p.ragged_kv = P->ragged ? 1 : 0;
+  p.ext_k = p.ext_v = nullptr;
+  p.ext_row_b = 0;
   p.wait_limit_k = (int32_t)((g_wait_limit.load(std::memory_order_relaxed) + 1023) >> 10);
   p.hold_wait = g_hold_wait.load(std::memory_order_relaxed);
   const float log2e = 1.4426950408889634f;
@@ -617,9 +622,11 @@ pkv::RunParams make_params(const pkv_plan* P, const void* q, const pkv_cache* c,
 int check_run(const pkv_plan* P, int mode, const void* q, const pkv_cache* c, void* o) {
   if (!P || !P->valid) return fail(PKV_EINVAL, "plan is NULL or has not been planned");
   if (!P->ws) return fail(PKV_EINVAL, "the plan is host-only (planned without a workspace)");
-  if (mode == PKV_MODE_RAGGED ? P->mode != PKV_MODE_RAGGED : (P->mode != mode && P->mode != PKV_MODE_MIXED))
+  if (mode == PKV_MODE_RAGGED || mode == PKV_MODE_PAGED_RAGGED ? P->mode != mode
+                                                             : (P->mode != mode && P->mode != PKV_MODE_MIXED))
     return fail(PKV_EINVAL, mode == PKV_MODE_DECODE    ? "decode_run needs a PKV_MODE_DECODE or PKV_MODE_MIXED plan"
                             : mode == PKV_MODE_RAGGED ? "ragged_run needs a PKV_MODE_RAGGED plan"
+                            : mode == PKV_MODE_PAGED_RAGGED ? "paged_ragged_run needs a PKV_MODE_PAGED_RAGGED plan"
                                                       : "prefill_run needs a PKV_MODE_PREFILL or PKV_MODE_MIXED plan");
   int st = pkv::check_cache(P, c);
   if (st != PKV_OK) return st;
@@ -807,7 +814,7 @@ namespace {
 // The prefill kernel over the plan's prefill items; `cache` is the pool (paged) or a one-token-page
 // view of the contiguous K/V tensors (ragged).
 int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* cache, void* o, float* lse,
-                void* stream, bool merge = false) {
+                void* stream, bool merge = false, const void* k_new = nullptr, const void* v_new = nullptr) {
   int st = check_run(plan, mode, q, cache, o);
   if (st != PKV_OK) return st;
   if (merge && !lse) return fail(PKV_EINVAL, "a merging run needs the held state's lse");
@@ -841,6 +848,11 @@ int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* 
   alignas(64) CUtensorMap tk{}, tv{};
   pkv::RunParams p = make_params(plan, q, cache, o, lse, first, count);
   p.merge_into = merge ? 1 : 0;
+  if (plan->paged_ragged) {
+    p.ext_k = static_cast<const char*>(k_new);
+    p.ext_v = static_cast<const char*>(v_new);
+    p.ext_row_b = (int64_t)plan->Hkv * plan->D * 2;
+  }
   PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
   const int64_t nm = (int64_t)plan->merge.size() - plan->num_decode_merge;
   if (nm > 0)
@@ -881,6 +893,16 @@ int pkv_attn_ragged_run(const pkv_plan* plan, const void* q, const void* k, cons
   view.k_scale = view.v_scale = 1.f;
   if (view.num_pages == 0) view.num_pages = 1;  // no rows read; keeps the tensor maps well formed
   return run_prefill(plan, PKV_MODE_RAGGED, q, &view, o, lse, stream);
+}
+
+int pkv_attn_paged_ragged_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, const void* k_new,
+                              const void* v_new, void* o, float* lse, void* stream) {
+  if (!plan || !plan->valid) return fail(PKV_EINVAL, "plan is NULL or has not been planned");
+  if (plan->mode != PKV_MODE_PAGED_RAGGED)
+    return fail(PKV_EINVAL, "paged_ragged_run needs a PKV_MODE_PAGED_RAGGED plan");
+  if (plan->total_tokens > 0 && (!k_new || !v_new)) return fail(PKV_EINVAL, "k_new and v_new must be non-NULL");
+  if (((uintptr_t)k_new | (uintptr_t)v_new) & 15) return fail(PKV_EINVAL, "k_new and v_new must be 16-byte aligned");
+  return run_prefill(plan, PKV_MODE_PAGED_RAGGED, q, cache, o, lse, stream, false, k_new, v_new);
 }
 
 int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,

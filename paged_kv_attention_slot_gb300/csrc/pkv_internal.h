@@ -92,6 +92,9 @@ struct RunParams {
   int32_t noncausal;   // prefill: 1 = every query sees all of its request's keys (0 = causal)
   int32_t ragged_kv;   // prefill: 1 = key j of request i is row page_base + j of the pools (no page table)
   int32_t merge_into;  // prefill: 1 = merge this pass's state into the state held in (o, lse) (LSE weights)
+  const char* ext_k;   // prefill over two sources: contiguous new-token K rows [tokens, Hkv, D] (else null)
+  const char* ext_v;
+  int64_t ext_row_b;   // bytes between consecutive new-token rows
   int32_t wait_limit_k;  // prefill: bound on each in-kernel wait, in units of 1024 SM clock cycles
   int32_t hold_wait;     // prefill: 1 = the MMA thread first waits on a barrier nothing arrives at (the
                          // wait runs out and the CTA takes its timeout path; a test of that path)
@@ -132,6 +135,7 @@ struct pkv_plan {
   int32_t mode = 0, batch = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, window_left = -1, kv_dtype = 0, q_dtype = 0;
   bool causal = true;   // false: every query sees all keys of its request (prefill / ragged plans)
   bool ragged = false;  // PKV_MODE_RAGGED: request i reads rows kv_indptr[i].. of contiguous K/V; max_page_id = last row
+  bool paged_ragged = false;  // PKV_MODE_PAGED_RAGGED: pages hold the prefix, the new rows come from k_new / v_new
   float sm_scale = 0.f;
   int64_t total_tokens = 0, max_page_id = -1, kv_tokens = 0, kv_chunk = 0, num_partials = 0;
   int64_t num_decode_work = 0;  // the decode kernel's items come first in `work`, the prefill kernel's after

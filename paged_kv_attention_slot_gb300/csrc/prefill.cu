@@ -121,6 +121,35 @@ __device__ __forceinline__ void add_scaled_bf16x8(const uint4& v, float w, float
   }
 }
 
+// One warp's share of a K or V tile: NW warps share the tile's 64 row pairs, this one (pw) copies
+// pairs pw, pw + NW, ...; in each cp.async lanes 0-15 copy the 16 chunks of the pair's first row and
+// lanes 16-31 those of its second, into the 128-byte-swizzled K-major layout (64-column halves).
+// Lane l holds the global addresses of the warp's rows l (ra) and 32 + l (rb); bit r of va / vb says
+// whether row r / 32 + r exists (else 16 zero bytes are written).  Fully unrolled: the destination of
+// pair i is a per-lane base plus a constant, because the swizzle of row 2 (pw + NW i) + hi repeats with
+// period 4 in i.
+template <int NW>
+__device__ __forceinline__ void issue_rows(uint32_t dst0, int pw, int pairs, uint64_t ra, uint64_t rb, uint32_t va,
+                                           uint32_t vb, int c, int hi) {
+  constexpr int MAXP = (pf::KT / 2 + NW - 1) / NW;
+  const int cc = c & 7;
+  const uint32_t va_l = va >> hi, vb_l = vb >> hi;
+  uint32_t base[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 2 * (pw + NW * k) + hi;
+    base[k] = dst0 + r * 128 + ((cc ^ (r & 7)) << 4);
+  }
+#pragma unroll
+  for (int i = 0; i < MAXP; ++i) {
+    if (i == MAXP - 1 && i >= pairs) break;  // only the last pair can be missing (V warps)
+    const uint64_t src = __shfl_sync(0xffffffffu, i < 16 ? ra : rb, (2 * i + hi) & 31);
+    const bool valid = ((i < 16 ? va_l : vb_l) >> ((2 * i) & 31)) & 1u;
+    const uint32_t dst = base[i & 3] + (uint32_t)((i >> 2) * 8 * NW * 128);
+    cp_async16(dst, reinterpret_cast<const char*>(src) + c * 16, valid ? 16u : 0u);
+  }
+}
+
 __global__ void __launch_bounds__(pf::THREADS, 1)
     prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, int32_t* err) {
@@ -218,54 +247,68 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       }
     }
     const int64_t head_off = (int64_t)w.kv_head * p.stride_head_b;
-    const int c = lane & 15;  // 16-byte chunk of the 256-byte row
-    const int half = c >> 3, cc = c & 7;
-    auto slot_of = [&](int key) -> int {
-      if (key >= w.kv_end) return -1;
+    const char* ext_base = is_k ? p.ext_k : p.ext_v;
+    const int64_t ext_head_off = (int64_t)w.kv_head * D * 2;
+    const int prefix = ri.kv_len - ri.q_len;  // keys before the request's first new token
+    const int ps = p.page_size;
+    const int ps_shift = (ps & (ps - 1)) == 0 ? __ffs(ps) - 1 : -1;
+    // Global address of the row holding `key` of this warp's operand, or null (no such key: the
+    // copy zero-fills).  Two-source plans take the keys from the prefix on from the contiguous
+    // new-token rows; ragged plans read row page_base + key; paged plans go through the page table.
+    auto row_addr = [&](int key) -> const char* {
+      if (key >= w.kv_end) return nullptr;
+      if (ext_base && key >= prefix) return ext_base + (int64_t)(ri.q_begin + key - prefix) * p.ext_row_b + ext_head_off;
+      int64_t slot;
       if (p.ragged_kv) {  // contiguous K/V: key j of the request is row page_base + j
-        const long long row = (long long)ri.page_base + key;
-        if (row >= p.num_pages) {
+        slot = (int64_t)ri.page_base + key;
+        if (slot >= p.num_pages) {
           record_error(err, PKV_DEVERR_PAGE_RANGE);
-          return -1;
+          return nullptr;
         }
-        return (int)row;
+      } else {
+        const int lp = ps_shift >= 0 ? key >> ps_shift : key / ps;
+        const int page = __ldg(p.kv_indices + ri.page_base + lp);
+        if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages) {
+          record_error(err, PKV_DEVERR_PAGE_RANGE);
+          return nullptr;
+        }
+        slot = (int64_t)page * ps + (key - lp * ps);
       }
-      const int lp = key / p.page_size;
-      const int page = __ldg(p.kv_indices + ri.page_base + lp);
-      if ((unsigned long long)(unsigned)page >= (unsigned long long)p.num_pages) {
-        record_error(err, PKV_DEVERR_PAGE_RANGE);
-        return -1;
-      }
-      return page * p.page_size + (key - lp * p.page_size);
+      return pool + slot * p.stride_token_b + head_off;
     };
-    bool ok = true;
-    // slot rows of the next tile are loaded one iteration ahead so their latency overlaps the copies;
-    // lane l holds the slots of this warp's rows l and 32 + l
+    // Lane l resolves the addresses of this warp's rows l and 32 + l of a tile one tile ahead (the
+    // page-table loads overlap the wait for the stage); a missing row reads from `pool` with a zero
+    // source size.  The validity bits of all lanes' rows travel as two ballots.
     const int nrows = 2 * pairs;
-    auto slot_idx = [&](int tile, int idx) -> int {
-      return idx < nrows ? slot_of(w.kv_begin + tile * KT + row_of(idx)) : -1;
+    struct Rows {
+      uint64_t a, b;
+      uint32_t va, vb;
     };
-    int next_a = slot_idx(0, lane);
-    int next_b = slot_idx(0, 32 + lane);
+    auto resolve = [&](int tile) -> Rows {
+      const int k0 = w.kv_begin + tile * KT;
+      const char* ra = lane < nrows ? row_addr(k0 + row_of(lane)) : nullptr;
+      const char* rb = 32 + lane < nrows ? row_addr(k0 + row_of(32 + lane)) : nullptr;
+      Rows r;
+      r.va = __ballot_sync(0xffffffffu, ra != nullptr);
+      r.vb = __ballot_sync(0xffffffffu, rb != nullptr);
+      r.a = (uint64_t)(ra ? ra : pool);
+      r.b = (uint64_t)(rb ? rb : pool);
+      return r;
+    };
+    const int c = lane & 15, hi = lane >> 4;  // 16-byte chunk of the 256-byte row; first or second row of a pair
+    bool ok = true;
+    Rows next = resolve(0);
     for (int j = 0; j < nkt && ok; ++j) {
       const int st = j & 1;
-      const int slot_a = next_a, slot_b = next_b;
-      if (j + 1 < nkt) {
-        next_a = slot_idx(j + 1, lane);
-        next_b = slot_idx(j + 1, 32 + lane);
-      }
+      const Rows cur = next;
+      if (j + 1 < nkt) next = resolve(j + 1);
       ok = __all_sync(0xffffffffu, tc::mbar_wait(empty0 + 8 * st, ((j >> 1) & 1) ^ 1, abort_flag, wait_limit));
       if (!ok) break;
-      const uint32_t dst0 = s_base + st * TILE_B + half * HALF_B;
-#pragma unroll 4
-      for (int i = 0; i < pairs; ++i) {
-        const int rr = 2 * i + (lane >> 4);  // index among this warp's rows
-        const int slot = __shfl_sync(0xffffffffu, i < 16 ? slot_a : slot_b, rr & 31);
-        const int row = row_of(rr);
-        const uint32_t dst = dst0 + row * 128 + ((cc ^ (row & 7)) << 4);
-        const char* src = pool + (slot >= 0 ? (int64_t)slot * p.stride_token_b + head_off + c * 16 : 0);
-        cp_async16(dst, src, slot >= 0 ? 16u : 0u);
-      }
+      const uint32_t dst0 = s_base + st * TILE_B + (c >> 3) * HALF_B;
+      if (is_k)
+        issue_rows<K_WARPS>(dst0, pw, pairs, cur.a, cur.b, cur.va, cur.vb, c, hi);
+      else
+        issue_rows<V_WARPS>(dst0, pw, pairs, cur.a, cur.b, cur.va, cur.vb, c, hi);
       // the stage's barrier receives this thread's arrival when its copies have landed; the MMA
       // thread fences them into the async proxy after its wait
       cp_async_arrive_noinc(full0 + 8 * st);

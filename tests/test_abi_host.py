@@ -632,3 +632,31 @@ def test_prefill_order_groups_requests_and_kv_heads_with_a_longest_first_tail(pk
     assert all(x >= y for x, y in zip(seq, seq[1:]))
     for s0, s1 in zip(starts, list(starts[1:]) + [cut]):
         assert np.all(np.diff(share[s0:s1]) <= share.max() // 64 + 1)
+
+
+def test_paged_ragged_plan_spans_prefix_and_new_rows(pk):
+    # PKV_MODE_PAGED_RAGGED: the page table holds only the prefix; each request's key range is its
+    # prefix plus its new tokens, planned exactly as the single causal paged pass over both
+    ps = 16
+    pre, n = [0, 100, 4096, 33], [50, 1, 300, 0]
+    npg = [(x + ps - 1) // ps for x in pre]
+    indptr = np.concatenate([[0], np.cumsum(npg)]).astype(np.int32)
+    indices = np.arange(indptr[-1], dtype=np.int32)
+    last = np.array([x - (k - 1) * ps if k else 0 for x, k in zip(pre, npg)], np.int32)
+    qo = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    kw = dict(num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=ps, num_sms=152, host_only=True)
+    p = pk.Plan().plan(qo, indptr, indices, last, mode="paged_ragged", **kw)
+    # the same batch as one paged pool holding prefix + new tokens
+    full = [x + y for x, y in zip(pre, n)]
+    fpg = [(x + ps - 1) // ps for x in full]
+    findptr = np.concatenate([[0], np.cumsum(fpg)]).astype(np.int32)
+    flast = np.array([x - (k - 1) * ps if k else 0 for x, k in zip(full, fpg)], np.int32)
+    f = pk.Plan().plan(qo, findptr, np.arange(findptr[-1], dtype=np.int32), flast, mode="prefill", **kw)
+    a, b = p.work_items(), f.work_items()
+    # same CTAs (request, KV head, key range, rows); only the page-list base differs
+    key = lambda it: sorted(map(tuple, it[:, [0, 1, 3, 4, 5, 7]].tolist()))
+    assert key(a) == key(b)
+    assert p.info()["kv_tokens"] == f.info()["kv_tokens"]
+    assert p.info()["max_page_id"] == int(indices.max())
+    # non-causal plans are allowed; decode-style checks do not apply
+    pk.Plan().plan(qo, indptr, indices, last, mode="paged_ragged", causal=False, **kw)

@@ -281,3 +281,85 @@ def test_extend_by_fused_merge_full_size_sampled():
     kp, vp, fmt = G.oracle_pools(b)
     ro, rl = G.oracle_attention(b, kp, vp, fmt, rows=rows)
     G.compare(out, lse, ro, rl, rows=rows)
+
+
+# ---- the same extend in ONE pass over two sources (PKV_MODE_PAGED_RAGGED) -------------------------
+def paged_ragged(b, g, **extra):
+    """One launch: each request's cached prefix through the prefix page table, its new tokens' K/V
+    from the contiguous k_new / v_new rows, one online softmax over both."""
+    pk = _pk()
+    pi, px, pl = prefix_csr(b)
+    p = pk.Plan().plan(b.qo_indptr, pi, px, pl, num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                       head_dim=b.head_dim, page_size=b.page_size, mode="paged_ragged", sm_scale=b.sm_scale,
+                       window_left=b.window_left, **extra)
+    out, lse = p.run_paged_ragged(g.q, g.cache, g.k_new, g.v_new, return_lse=True)
+    torch.cuda.synchronize()
+    return out, lse, p
+
+
+def _new_rows_differ_from_pool(b):
+    """The pool's slots for the new tokens hold other values than k_new (so a kernel reading them from
+    the pool instead of k_new would fail the comparison)."""
+    P, ps, H, D = b.k_pool.shape
+    k = b.k_pool.view(P * ps, H, D)[torch.from_numpy(b.slot_mapping)]
+    return not torch.equal(k, b.k_new)
+
+
+@pytest.mark.parametrize("ps", [1, 16, 64])
+def test_paged_ragged_one_pass_reads_new_rows_from_the_contiguous_tensors(ps):
+    # the pool is NOT written with this step's K/V first: the new keys can only come from k_new / v_new;
+    # the result is the oracle's causal pass over prefix + new tokens (the oracle's pool is written)
+    b = W.make_batch([700, 129, 64, 1000, 90, 33], [300, 129, 1, 37, 0, 33], ps, 32, 8, 128, seed=100 + ps)
+    assert _new_rows_differ_from_pool(b)
+    g = G.GpuBatch(b)
+    out, lse, p = paged_ragged(b, g)
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt)
+    G.compare(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("hq, hkv, window", [(8, 8, -1), (16, 2, -1), (128, 1, -1), (32, 8, 0), (32, 8, 100)])
+def test_paged_ragged_gqa_and_windows(hq, hkv, window):
+    b = W.make_batch([500, 40, 1300], [200, 40, 129], 16, hq, hkv, 128, seed=110 + hq + window, window_left=window)
+    g = G.GpuBatch(b)
+    out, lse, p = paged_ragged(b, g)
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt)
+    G.compare(out, lse, ro, rl)
+
+
+def test_paged_ragged_noncausal_and_split():
+    # causal=False: every new token sees the whole prefix and every new token of its request; and a
+    # long prefix with few queries, split into key chunks (the chunks may straddle the two sources)
+    pk = _pk()
+    b = W.make_batch([300, 9000, 45], [60, 48, 45], 16, 32, 8, 128, seed=120)
+    g = G.GpuBatch(b)
+    kp, vp, fmt = G.oracle_pools(b)
+    out, lse, p = paged_ragged(b, g, causal=False)
+    ro, rl = OA.paged_attention(G.bf16_bits(b.q), kp, vp, b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len,
+                                b.page_size, q_format="bf16_bits", kv_format=fmt, causal=False)
+    G.compare(out, lse, ro, rl)
+    out, lse, p = paged_ragged(b, g, num_sms=4096)
+    assert p.info()["num_prefill_partials"] > 0
+    ro, rl = G.oracle_attention(b, kp, vp, fmt)
+    G.compare(out, lse, ro, rl)
+
+
+def test_paged_ragged_full_size_prefix_extend():
+    # the prefix-cached extend workload in the benchmark's launch: every row of the longest and the
+    # shortest request, sampled rows of the others
+    b = W.workload(3)
+    g = G.GpuBatch(b)
+    out, lse, p = paged_ragged(b, g)
+    rng = np.random.default_rng(5)
+    n = np.diff(b.qo_indptr)
+    whole = {int(np.argmax(n)), int(np.argmin(n))}
+    rows = []
+    for i in range(b.batch_size):
+        q0, q1 = int(b.qo_indptr[i]), int(b.qo_indptr[i + 1])
+        rows += list(range(q0, q1)) if i in whole else [q0, q1 - 1] + rng.integers(q0, q1, size=3).tolist()
+    rows = sorted(set(rows))
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt, rows=rows)
+    G.compare(out, lse, ro, rl, rows=rows)
+    assert p.info()["num_work"] > 1000
