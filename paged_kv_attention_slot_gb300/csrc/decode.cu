@@ -150,37 +150,6 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
       }
     }
   }
-  // FP8 KV runs the products in f16, whose largest finite value is 65504: a larger |q| would become
-  // inf.  The CTA's Q rows are scaled by 2^-e, with e the smallest power that brings max |q| below
-  // 2^15, and the score scale is multiplied by 2^e.  The scaling is exact (a bf16 value inside the f16
-  // normal range is an f16 value), and e = 0 whenever max |q| < 2^15.
-  float sc = p.scale_log2;
-  if constexpr (FP8) {
-    uint32_t amax = 0;  // largest |q| as bf16 magnitude bits (monotonic in the value)
-#pragma unroll
-    for (int ks = 0; ks < C::KS; ++ks)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t r = qb[ks][nb][h];
-          amax = max(amax, max(r & 0x7fffu, (r >> 16) & 0x7fffu));
-        }
-    amax = __reduce_max_sync(0xffffffffu, amax);  // every warp holds the CTA's whole Q
-    const int e = max(0, (int)(amax >> 7) - 127 - 14);  // bf16 exponent field -> floor(log2 max |q|)
-    const float down = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 114: a normal float)
-    sc *= __uint_as_float((uint32_t)(127 + e) << 23);              // 2^e
-#pragma unroll
-    for (int ks = 0; ks < C::KS; ++ks)
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t r = qb[ks][nb][h];
-          qb[ks][nb][h] = pack_f16(__uint_as_float(r << 16) * down, __uint_as_float(r & 0xffff0000u) * down);
-        }
-  }
-
   // ---- per-warp cp.async ring ----
   uint8_t* wsm = smem + warp * C::WARP_SMEM;
   const uint32_t wsm_u = smem_u32(wsm);
@@ -290,6 +259,38 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     if (lane == 0) key_of_stage[s] = lkey;
     if (lkey < w.kv_end) load_tile(s);
     cp_async_commit();
+  }
+
+  // (Done here, after the first tiles' copies are issued, so the Q loads overlap them.)
+  // FP8 KV runs the products in f16, whose largest finite value is 65504: a larger |q| would become
+  // inf.  The CTA's Q rows are scaled by 2^-e, with e the smallest power that brings max |q| below
+  // 2^15, and the score scale is multiplied by 2^e.  The scaling is exact (a bf16 value inside the f16
+  // normal range is an f16 value), and e = 0 whenever max |q| < 2^15.
+  float sc = p.scale_log2;
+  if constexpr (FP8) {
+    uint32_t amax = 0;  // largest |q| as bf16 magnitude bits (monotonic in the value)
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t r = qb[ks][nb][h];
+          amax = max(amax, max(r & 0x7fffu, (r >> 16) & 0x7fffu));
+        }
+    amax = __reduce_max_sync(0xffffffffu, amax);  // every warp holds the CTA's whole Q
+    const int e = max(0, (int)(amax >> 7) - 127 - 14);  // bf16 exponent field -> floor(log2 max |q|)
+    const float down = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e (e <= 114: a normal float)
+    sc *= __uint_as_float((uint32_t)(127 + e) << 23);              // 2^e
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks)
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t r = qb[ks][nb][h];
+          qb[ks][nb][h] = pack_f16(__uint_as_float(r << 16) * down, __uint_as_float(r & 0xffff0000u) * down);
+        }
   }
 
   // ldmatrix lane roles: K as the A operand (rows = keys), V^T as the A operand (.trans, rows = dims)
