@@ -143,6 +143,25 @@ def test_decode_fp8_query_beyond_the_f16_range():
     G.compare(out, lse, ro, rl, max_abs=G.FP8_MAX_ABS, lse_rel=1e-6)
 
 
+@pytest.mark.parametrize("kv, num_sms", [("bf16", 16), ("bf16", 64), ("bf16", 600), ("e4m3", 600)])
+def test_decode_split_merges_up_to_hundreds_of_partials(kv, num_sms):
+    # a 100,000-key request split over 16, ~60 or ~390 CTAs (the last CTA of the unit merges them all,
+    # in chunks that fit its shared memory), shorter requests with fewer or no splits; every element
+    # against the oracle
+    ps = 16 if kv == "bf16" else 128
+    b = W.make_batch([100000, 3000, 200, 17], [1, 1, 1, 1], ps, 8, 2, 128, seed=130, kv_dtype=kv)
+    stats, plan = _decode_case(b, num_sms=num_sms)
+    splits = np.bincount(plan.work_items()[:, 0] * 2 + plan.work_items()[:, 1])
+    assert splits.max() > 12 and plan.info()["num_merge"] > 0
+    # and a second run of the same plan (the group and unit counters were returned to zero)
+    g = G.GpuBatch(b)
+    g.store()
+    out, lse = g.run(plan)
+    kp, vp, fmt = G.oracle_pools(b)
+    ro, rl = G.oracle_attention(b, kp, vp, fmt)
+    G.compare(out, lse, ro, rl, max_abs=G.FP8_MAX_ABS if kv == "e4m3" else G.BF16_MAX_ABS)
+
+
 def test_decode_tiny_workload_all_elements():
     stats, plan = _decode_case(W.workload(1))
     assert plan.info()["num_merge"] == 0
