@@ -660,3 +660,25 @@ def test_paged_ragged_plan_spans_prefix_and_new_rows(pk):
     assert p.info()["max_page_id"] == int(indices.max())
     # non-causal plans are allowed; decode-style checks do not apply
     pk.Plan().plan(qo, indptr, indices, last, mode="paged_ragged", causal=False, **kw)
+
+
+def test_paged_ragged_argument_checks(pk):
+    import ctypes as C
+
+    L = pk._lib.lib()
+    kw = dict(num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=16, num_sms=152, host_only=True)
+    args = ([0, 40], [0, 3], [0, 1, 2], [16])
+    p = pk.Plan().plan(*args, mode="paged_ragged", **kw)
+    f = pk.Plan().plan(*args, mode="prefill", **kw)
+    cache = pk._lib.pkv_cache(16, 16, 4, 16, 2, 128, 0, 4096, 256, 128, 1.0, 1.0)
+    # a prefill plan cannot run as paged + ragged, nor a paged + ragged plan as prefill
+    assert L.pkv_attn_paged_ragged_run(f._h, 16, C.byref(cache), 16, 16, 16, None, None) == pk._lib.PKV_EINVAL
+    assert "PKV_MODE_PAGED_RAGGED" in L.pkv_last_error().decode()
+    assert L.pkv_attn_prefill_run(p._h, 16, C.byref(cache), 16, None, None) == pk._lib.PKV_EINVAL
+    # the new rows are required and must be 16-byte aligned
+    assert L.pkv_attn_paged_ragged_run(p._h, 16, C.byref(cache), None, 16, 16, None, None) == pk._lib.PKV_EINVAL
+    assert L.pkv_attn_paged_ragged_run(p._h, 16, C.byref(cache), 24, 16, 16, None, None) == pk._lib.PKV_EINVAL
+    # the prefill kernel reads a bf16 cache only
+    with pytest.raises(pk.PkvError) as ei:
+        pk.Plan().plan(*args, mode="paged_ragged", kv_dtype="e4m3", **kw)
+    assert ei.value.args[0].startswith("PKV_EUNSUPPORTED")
