@@ -11,14 +11,17 @@
 // GB300 design.  One CTA = two 128-row query tiles (A and B: consecutive tokens of one request, rows
 // = (token, head) pairs of one KV head's query-head group) sharing every K/V tile, so each gathered
 // K/V byte feeds twice the tensor-core work of a single tile:
-//  * warps 8-11 and 13-15 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps 8,
-//    9, 13, 14) and V (warps 10, 11, 15) tiles of 128 keys gathered row by row through the page table
-//    with 16-byte cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the
-//    tensor core reads; two stages.  Each producer thread's arrival on the stage's mbarrier is posted
-//    by the hardware when its copies land (cp.async.mbarrier.arrive.noinc), so a tile is announced as
-//    soon as it is in shared memory; the MMA thread fences it into the async proxy after its wait.
-//    A warp stalls on each cp.async it issues, so the gather is spread over seven warps.  (TMA
-//    tile::gather4 moves 512 bytes per instruction and measured slower here for token-granular pools.)
+//  * warps 8-11 and 13-15 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps
+//    8-11) and V (warps 13-15) tiles of 128 keys gathered row by row through the page table with
+//    16-byte cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the
+//    tensor core reads; two stages.  Each lane resolves the global addresses of two of its warp's
+//    rows of the next tile while the stage is still in use, so the unrolled copy loop spends one
+//    shuffle, a bit test and an add per cp.async: the producers share the schedulers with the softmax
+//    warps, and their instruction count sets the pace of the gather.  Each producer thread's arrival
+//    on the stage's mbarrier is posted by the hardware when its copies land
+//    (cp.async.mbarrier.arrive.noinc), so a tile is announced as soon as it is in shared memory; the
+//    MMA thread fences it into the async proxy after its wait.  (TMA tile::gather4 moves 512 bytes
+//    per instruction and measured slower here for token-granular pools.)
 //  * warp 12 (MMA): one thread issues tcgen05.mma (kind::f16, M=128, N=128, K=16, bf16 in, fp32
 //    accumulate in TMEM) in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ..., so the
 //    tensor core works on one tile while the other tile's softmax runs.  P lives in TMEM on top of
@@ -81,8 +84,9 @@ constexpr uint32_t TMEM_O = 256;
 constexpr int THREADS = 512;          // 4 warpgroups: softmax A, softmax B, producers, MMA + producers
 constexpr int PRODUCER_WARP0 = 8;     // warps 8-11 and 13-15 gather K and V
 constexpr int MMA_WARP = 12;
-// Producer roles: K by warps 8, 9, 13, 14 and V by warps 10, 11, 15 (K is needed first, by S).
-// Every warp stalls on each cp.async it issues, so the gather of a tile is spread over all seven.
+// Producer roles: K by warps 8-11 and V by warps 13-15 (K is needed first, by S).  Warp w runs on
+// scheduler w % 4, so each of schedulers 1-3 carries one K and one V warp (16 + 21-22 row pairs a
+// tile) and scheduler 0, which also runs the MMA thread, one K warp.
 constexpr int K_WARPS = 4, V_WARPS = 3;
 // launched at 65536 / 512 = 128 registers per thread, then rebalanced per warpgroup:
 // 2 x 128 x SOFTMAX_REGS + 2 x 128 x OTHER_REGS = 47104 + 18432 = 65536 <= 65536
@@ -227,8 +231,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc::reg_dealloc<OTHER_REGS>();
     // role: operand and index among that operand's warps; warp k of n copies the row pairs
     // q = k, k + n, k + 2n, ... (rows 2q and 2q + 1, 16 lanes per 256-byte row)
-    const bool is_k = warp == 8 || warp == 9 || warp == 13 || warp == 14;
-    const int pw = warp == 8 || warp == 10 ? 0 : warp == 9 || warp == 11 ? 1 : warp == 13 || warp == 15 ? 2 : 3;
+    const bool is_k = warp < MMA_WARP;  // K: warps 8-11, V: warps 13-15
+    const int pw = is_k ? warp - PRODUCER_WARP0 : warp - MMA_WARP - 1;
     const int nw = is_k ? K_WARPS : V_WARPS;
     const int pairs = (KT / 2 - pw + nw - 1) / nw;  // row pairs of this warp per tile
     auto row_of = [&](int idx) -> int { return 2 * (pw + nw * (idx >> 1)) + (idx & 1); };  // idx-th row
