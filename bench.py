@@ -680,7 +680,8 @@ def next_rows_measure(device, peak_tflops, hbm):
         "flat_gbs": round(flat_bytes / (flat_ms * 1e-3) / 1e9, 1),
         "cascade_unique_gbs": round(unique_bytes / (cas_ms * 1e-3) / 1e9, 1),
         "cascade_equivalent_gbs": round(flat_bytes / (cas_ms * 1e-3) / 1e9, 1),
-        "launches": 4, "timing": mode,
+        "launches": 2 + (1 if cas.shared.info()["num_prefill_partials"] else 0), "timing": mode,
+        "how": "pkv_cascade_run: the suffix decode into (o, lse), then the shared non-causal pass merged in its epilogue",
         "plans": {"shared_ctas": cas.shared.info()["num_work"], "suffix_ctas": cas.suffix.info()["num_work"]}}
     del st, flat, cas, lse
     torch.cuda.empty_cache()

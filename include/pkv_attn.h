@@ -305,6 +305,26 @@ int pkv_attn_ragged_run(const pkv_plan* plan, const void* q, const void* k, cons
 int pkv_attn_paged_ragged_run(const pkv_plan* plan, const void* q, const pkv_cache* cache, const void* k_new,
                               const void* v_new, void* o, float* lse, void* stream);
 
+/*
+ * pkv_cascade_run: attention of a batch whose requests share a prefix, with the shared part computed
+ * once ("vLLM 源码完全拆解（六）：Attention Backend", section «Cascade Attention 把共享前缀只算一次»: each
+ * query's attention is split into the shared prefix and its request's own suffix, and the two results
+ * are combined by their log-sum-exp weights).
+ *   shared  a non-causal (causal == 0) PKV_MODE_PREFILL plan over the shared prefix's pages whose
+ *           query rows are every row of the batch (normally one "request": qo_indptr = {0, T});
+ *   suffix  a plan over each request's own pages after the shared prefix (holding its new tokens):
+ *           PKV_MODE_DECODE, PKV_MODE_PREFILL or PKV_MODE_MIXED, with the same head counts, head_dim and
+ *           total_tokens T as `shared`;
+ *   q, cache  as pkv_attn_prefill_run (one pool holds both levels' pages);
+ *   o, lse  device bf16 [T, Hq, D] and fp32 [T, Hq] (lse is required: the merge needs it).
+ * The suffix plan's runs write (o, lse), then the shared pass runs with its state merged into them
+ * in its epilogue (pkv_attn_prefill_run_merge): two launches, three with a decode/prefill-mixed suffix
+ * or a split shared pass, and no scratch.  Errors as the runs it makes; nothing is enqueued when the
+ * plans do not match.
+ */
+int pkv_cascade_run(const pkv_plan* shared, const pkv_plan* suffix, const void* q, const pkv_cache* cache, void* o,
+                    float* lse, void* stream);
+
 int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
                     int64_t num_states, int32_t head_dim, void* stream);
 

@@ -331,14 +331,13 @@ class CascadePlan:
     which a single "request" holds every query row of the batch and the shared pages (so each
     shared K/V tile is read once per query tile instead of once per request); level 1 is an ordinary
     causal plan over each request's own suffix pages (decode when every request has one new token).
-    The run is three library calls: level 0 into ``out``/``lse``, level 1 into buffers kept by this
-    object, and pkv_merge_state in place.
+    The run is one library call, pkv_cascade_run: level 1 into ``out``/``lse``, then level 0 with
+    its state merged into them in its epilogue.
     """
 
     def __init__(self):
         self.shared = Plan()
         self.suffix = Plan()
-        self._o2 = self._s2 = None
 
     def plan(self, qo_indptr, shared_kv_indices, shared_last_page_len: int, kv_indptr, kv_indices, last_page_len, *,
              num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale=0.0, num_sms=0, max_splits=0,
@@ -359,35 +358,14 @@ class CascadePlan:
         self.total_tokens = T
         return self
 
-    def run_paged_ragged(self, q: torch.Tensor, cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
-                         out: torch.Tensor | None = None, lse: torch.Tensor | None = None, return_lse: bool = False,
-                         stream=None):
-        """Attention of a "paged_ragged" plan in one pass: the page table holds each request's cached
-        prefix in `cache`; k_new, v_new are contiguous bf16 [total_tokens, num_kv_heads, head_dim] holding
-        the new tokens' K / V (row r = token r of q)."""
-        if self.mode != "paged_ragged":
-            raise ValueError("run_paged_ragged needs a plan made with mode='paged_ragged'")
-        for name, t in (("k_new", k_new), ("v_new", v_new)):
-            if t.dtype != torch.bfloat16 or not t.is_contiguous():
-                raise ValueError(f"{name} must be a contiguous bf16 tensor")
-            if tuple(t.shape) != (self.total_tokens, self.num_kv_heads, self.head_dim):
-                raise ValueError(f"{name} must be [{self.total_tokens}, {self.num_kv_heads}, {self.head_dim}]")
-        out, lse = self._outputs(q, out, lse, return_lse)
-        check(lib().pkv_attn_paged_ragged_run(self._h, q.data_ptr(), C.byref(cache.struct), k_new.data_ptr(),
-                                              v_new.data_ptr(), out.data_ptr(),
-                                              lse.data_ptr() if lse is not None else None, _stream_ptr(stream)))
-        return (out, lse) if (return_lse or lse is not None) else out
-
     def run(self, q: torch.Tensor, cache: KVCache, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
             return_lse: bool = False, stream=None):
+        """pkv_cascade_run: the suffix plan into (out, lse), then the shared pass merged into them."""
         if lse is None:
             lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
-        out, lse = self.shared.run(q, cache, out=out, lse=lse, stream=stream)
-        if self._o2 is None or self._o2.shape != q.shape or self._o2.device != q.device:
-            self._o2 = torch.empty_like(q)
-            self._s2 = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
-        self.suffix.run(q, cache, out=self._o2, lse=self._s2, stream=stream)
-        merge_state(out, lse, self._o2, self._s2, out=out, lse_out=lse, stream=stream)
+        out, lse = self.suffix._outputs(q, out, lse, True)
+        check(lib().pkv_cascade_run(self.shared._h, self.suffix._h, q.data_ptr(), C.byref(cache.struct),
+                                    out.data_ptr(), lse.data_ptr(), _stream_ptr(stream)))
         return (out, lse) if return_lse else out
 
 

@@ -116,6 +116,8 @@ _SIGS = {
     "pkv_attn_ragged_run": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]),
     "pkv_attn_paged_ragged_run": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p,
                                             C.c_void_p, C.c_void_p, C.c_void_p]),
+    "pkv_cascade_run": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(pkv_cache), C.c_void_p, C.c_void_p,
+                                  C.c_void_p]),
     "pkv_merge_state": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64,
                                   C.c_int32, C.c_void_p]),
     "pkv_last_error": (C.c_char_p, []),

@@ -905,6 +905,33 @@ int pkv_attn_paged_ragged_run(const pkv_plan* plan, const void* q, const pkv_cac
   return run_prefill(plan, PKV_MODE_PAGED_RAGGED, q, cache, o, lse, stream, false, k_new, v_new);
 }
 
+int pkv_cascade_run(const pkv_plan* shared, const pkv_plan* suffix, const void* q, const pkv_cache* cache, void* o,
+                    float* lse, void* stream) {
+  if (!shared || !suffix || !shared->valid || !suffix->valid)
+    return fail(PKV_EINVAL, "both plans must be planned");
+  if (shared->mode != PKV_MODE_PREFILL || shared->causal)
+    return fail(PKV_EINVAL, "the shared plan must be a non-causal PKV_MODE_PREFILL plan");
+  if (suffix->mode != PKV_MODE_DECODE && suffix->mode != PKV_MODE_PREFILL && suffix->mode != PKV_MODE_MIXED)
+    return fail(PKV_EINVAL, "the suffix plan must be a PKV_MODE_DECODE, PREFILL or MIXED plan");
+  if (shared->Hq != suffix->Hq || shared->Hkv != suffix->Hkv || shared->D != suffix->D ||
+      shared->total_tokens != suffix->total_tokens)
+    return fail(PKV_EINVAL, "the shared and suffix plans must have the same heads, head_dim and query rows");
+  if (shared->total_tokens > 0 && !lse) return fail(PKV_EINVAL, "lse is required (the levels merge by it)");
+  // every check of both runs before anything is enqueued
+  int st = check_run(suffix, suffix->mode == PKV_MODE_DECODE ? PKV_MODE_DECODE : PKV_MODE_PREFILL, q, cache, o);
+  if (st == PKV_OK) st = check_run(shared, PKV_MODE_PREFILL, q, cache, o);
+  if (st != PKV_OK) return st;
+  if (suffix->num_decode_work > 0) {
+    st = pkv_attn_decode_run(suffix, q, cache, o, lse, stream);
+    if (st != PKV_OK) return st;
+  }
+  if ((int64_t)suffix->work.size() > suffix->num_decode_work) {
+    st = run_prefill(suffix, PKV_MODE_PREFILL, q, cache, o, lse, stream);
+    if (st != PKV_OK) return st;
+  }
+  return run_prefill(shared, PKV_MODE_PREFILL, q, cache, o, lse, stream, true);
+}
+
 int pkv_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o, float* lse,
                     int64_t num_states, int32_t head_dim, void* stream) {
   if (num_states < 0) return fail(PKV_EINVAL, "num_states < 0");

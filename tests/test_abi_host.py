@@ -682,3 +682,27 @@ def test_paged_ragged_argument_checks(pk):
     with pytest.raises(pk.PkvError) as ei:
         pk.Plan().plan(*args, mode="paged_ragged", kv_dtype="e4m3", **kw)
     assert ei.value.args[0].startswith("PKV_EUNSUPPORTED")
+
+
+def test_cascade_run_argument_checks(pk):
+    # pkv_cascade_run: a non-causal prefill plan over the shared pages for every query row, and a
+    # suffix plan over the same rows; mismatches fail before anything is enqueued
+    import ctypes as C
+
+    L = pk._lib.lib()
+    kw = dict(num_kv_heads=2, head_dim=128, page_size=16, num_sms=152, host_only=True)
+    shared = pk.Plan().plan([0, 3], [0, 4], [0, 1, 2, 3], [16], num_qo_heads=8, mode="prefill", causal=False, **kw)
+    causal_shared = pk.Plan().plan([0, 3], [0, 4], [0, 1, 2, 3], [16], num_qo_heads=8, mode="prefill", **kw)
+    suffix = pk.Plan().plan([0, 1, 2, 3], [0, 1, 2, 3], [4, 5, 6], [3, 7, 16], num_qo_heads=8, mode="decode", **kw)
+    other_heads = pk.Plan().plan([0, 1, 2, 3], [0, 1, 2, 3], [4, 5, 6], [3, 7, 16], num_qo_heads=16, mode="decode", **kw)
+    two_rows = pk.Plan().plan([0, 1, 2], [0, 1, 2], [4, 5], [3, 7], num_qo_heads=8, mode="decode", **kw)
+    cache = pk._lib.pkv_cache(16, 16, 8, 16, 2, 128, 0, 4096, 256, 128, 1.0, 1.0)
+    run = lambda a, b, lse=16: L.pkv_cascade_run(a._h, b._h, 16, C.byref(cache), 16, lse, None)  # noqa: E731
+    for a, b, msg in [(causal_shared, suffix, "non-causal"), (shared, other_heads, "same heads"),
+                      (shared, two_rows, "same heads"), (suffix, suffix, "non-causal")]:
+        assert run(a, b) == pk._lib.PKV_EINVAL
+        assert msg in L.pkv_last_error().decode()
+    assert run(shared, suffix, lse=None) == pk._lib.PKV_EINVAL
+    assert "lse is required" in L.pkv_last_error().decode()
+    assert run(shared, suffix) == pk._lib.PKV_EINVAL  # host-only plans cannot run
+    assert "host-only" in L.pkv_last_error().decode()
