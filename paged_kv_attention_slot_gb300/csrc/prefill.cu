@@ -581,8 +581,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
 // of the item's two tiles (the prefill kernel's (token, head) order).  m = max_s lse_s, w_s =
 // 2^(lse_s - m) / sum_s 2^(lse_s - m), o = sum_s w_s o_s; a row whose chunks saw no key gets o = 0 and
 // lse = -inf.  Few items (a shared prefix, a few long requests) take one group per CTA so that the
-// grid still covers the SMs.  A merging run (the result merged into the state held in (o, lse)) uses
-// one CTA per item, so that each row's held lse is read and rewritten by one thread.
+// grid still covers the SMs.  In a merging run (the result merged into the state held in (o, lse)) every
+// slice reads a row's held lse and the last slice of the item to finish (a per-item counter) rewrites
+// it, so no slice can read a merged lse.
 template <int G4>
 __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const RunParams p, int64_t first_merge) {
   const MergeItem m = p.merge[first_merge + blockIdx.x];
@@ -591,56 +592,75 @@ __global__ void __launch_bounds__(kPrefillItemRows) prefill_merge_kernel(const R
   const int T = pf::ROWS / G;
   const int x = r / pf::ROWS, rr = r % pf::ROWS;
   const int t = x * T + rr / G, g = rr % G;
-  if (t >= m.q_rows) return;
-  const float* lse_s = p.ppart_lse + (int64_t)m.first_slot * kPrefillItemRows + r;
-  float mx = -INFINITY;
-  for (int sp = 0; sp < m.num_splits; ++sp) mx = fmaxf(mx, lse_s[(int64_t)sp * kPrefillItemRows]);
-  float sum = 0.f;
-  if (mx != -INFINITY)
-    for (int sp = 0; sp < m.num_splits; ++sp) sum += ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
+  const bool valid = t < m.q_rows;  // rows past the item's tokens do nothing (no early exit: barriers below)
   const int64_t row = (int64_t)(m.q_row + t);
   const int head = m.kv_head * G + g;
-  // the merged state of the pieces; merged in turn into the held (o, lse) when the run merges
-  float lse_out = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
-  float w_prev = 0.f, w_this = 1.f;
-  if (p.merge_into) merge_weights(p.lse[row * p.num_qo_heads + head], lse_out, w_prev, w_this);
-  const float inv = (sum > 0.f ? 1.f / sum : 0.f) * w_this;
-  const int per_cta = 32 / gridDim.y;  // four-column groups of this CTA
-  uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D);
-  for (int g0 = blockIdx.y * per_cta; g0 < (blockIdx.y + 1) * per_cta; g0 += G4) {
-    float4 acc[G4];
+  float lse_out = -INFINITY;
+  if (valid) {
+    const float* lse_s = p.ppart_lse + (int64_t)m.first_slot * kPrefillItemRows + r;
+    float mx = -INFINITY;
+    for (int sp = 0; sp < m.num_splits; ++sp) mx = fmaxf(mx, lse_s[(int64_t)sp * kPrefillItemRows]);
+    float sum = 0.f;
+    if (mx != -INFINITY)
+      for (int sp = 0; sp < m.num_splits; ++sp) sum += ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
+    // the merged state of the pieces; merged in turn into the held (o, lse) when the run merges
+    lse_out = sum > 0.f ? (mx + __log2f(sum)) * 0.69314718055994531f : -INFINITY;
+    float w_prev = 0.f, w_this = 1.f;
+    if (p.merge_into) merge_weights(p.lse[row * p.num_qo_heads + head], lse_out, w_prev, w_this);
+    const float inv = (sum > 0.f ? 1.f / sum : 0.f) * w_this;
+    const int per_cta = 32 / gridDim.y;  // four-column groups of this CTA
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * pf::D);
+    for (int g0 = blockIdx.y * per_cta; g0 < (blockIdx.y + 1) * per_cta; g0 += G4) {
+      float4 acc[G4];
 #pragma unroll
-    for (int c = 0; c < G4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (mx != -INFINITY) {
-      for (int sp = 0; sp < m.num_splits; ++sp) {
-        const float wgt = ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
-        const float4* src = reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) *
-                                                                            kPrefillPartialFloats) +
-                            g0 * kPrefillItemRows + r;
+      for (int c = 0; c < G4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (mx != -INFINITY) {
+        for (int sp = 0; sp < m.num_splits; ++sp) {
+          const float wgt = ex2(lse_s[(int64_t)sp * kPrefillItemRows] - mx);
+          const float4* src = reinterpret_cast<const float4*>(p.ppart_o + (int64_t)(m.first_slot + sp) *
+                                                                              kPrefillPartialFloats) +
+                              g0 * kPrefillItemRows + r;
 #pragma unroll
-        for (int c = 0; c < G4; ++c) {
-          const float4 v = src[c * kPrefillItemRows];
-          acc[c].x = fmaf(wgt, v.x, acc[c].x);
-          acc[c].y = fmaf(wgt, v.y, acc[c].y);
-          acc[c].z = fmaf(wgt, v.z, acc[c].z);
-          acc[c].w = fmaf(wgt, v.w, acc[c].w);
+          for (int c = 0; c < G4; ++c) {
+            const float4 v = src[c * kPrefillItemRows];
+            acc[c].x = fmaf(wgt, v.x, acc[c].x);
+            acc[c].y = fmaf(wgt, v.y, acc[c].y);
+            acc[c].z = fmaf(wgt, v.z, acc[c].z);
+            acc[c].w = fmaf(wgt, v.w, acc[c].w);
+          }
         }
       }
-    }
 #pragma unroll
-    for (int c = 0; c < G4; ++c) {
-      float f[4] = {acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv};
-      if (p.merge_into) {
-        const uint2 prev = dst[g0 + c];
-        f[0] = fmaf(w_prev, __uint_as_float(prev.x << 16), f[0]);
-        f[1] = fmaf(w_prev, __uint_as_float(prev.x & 0xffff0000u), f[1]);
-        f[2] = fmaf(w_prev, __uint_as_float(prev.y << 16), f[2]);
-        f[3] = fmaf(w_prev, __uint_as_float(prev.y & 0xffff0000u), f[3]);
+      for (int c = 0; c < G4; ++c) {
+        float f[4] = {acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv};
+        if (p.merge_into) {
+          const uint2 prev = dst[g0 + c];
+          f[0] = fmaf(w_prev, __uint_as_float(prev.x << 16), f[0]);
+          f[1] = fmaf(w_prev, __uint_as_float(prev.x & 0xffff0000u), f[1]);
+          f[2] = fmaf(w_prev, __uint_as_float(prev.y << 16), f[2]);
+          f[3] = fmaf(w_prev, __uint_as_float(prev.y & 0xffff0000u), f[3]);
+        }
+        dst[g0 + c] = make_uint2(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]));
       }
-      dst[g0 + c] = make_uint2(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]));
     }
   }
-  if (p.lse && blockIdx.y == 0) p.lse[row * p.num_qo_heads + head] = lse_out;
+  if (!p.lse) return;
+  if (!p.merge_into) {
+    if (valid && blockIdx.y == 0) p.lse[row * p.num_qo_heads + head] = lse_out;
+    return;
+  }
+  // merging run: every slice has read the held lse of its rows before the last slice of the item to
+  // finish rewrites them; its counter is zero before the run and again after it
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(p.unit_count + first_merge + blockIdx.x, 1) == (int)gridDim.y - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  if (valid) p.lse[row * p.num_qo_heads + head] = lse_out;
+  if (threadIdx.x == 0) p.unit_count[first_merge + blockIdx.x] = 0;
 }
 
 cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s) {
@@ -648,9 +668,7 @@ cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  if (p.merge_into)
-    prefill_merge_kernel<4><<<dim3((unsigned)count, 1), kPrefillItemRows, 0, s>>>(p, first_merge);
-  else if (count * 8 >= 2 * (int64_t)sms)
+  if (count * 8 >= 2 * (int64_t)sms)
     prefill_merge_kernel<4><<<dim3((unsigned)count, 8), kPrefillItemRows, 0, s>>>(p, first_merge);
   else
     prefill_merge_kernel<1><<<dim3((unsigned)count, 32), kPrefillItemRows, 0, s>>>(p, first_merge);
