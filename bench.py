@@ -463,50 +463,62 @@ def kernel_ms(run_once, reps=20, iters=7):
 
 
 def run_e2e(b, st, plan, steps, warmup):
-    """Same step through the public API from pinned HOST buffers: H2D of the step's inputs, D2H of O."""
+    """Same step through the public API from pinned HOST buffers: every step copies its inputs (Q,
+    the new K/V rows, slot_mapping) host -> device, re-plans, writes the KV, runs, and copies O back
+    to the host.  Steps are pipelined as a serving loop would: the host plans and enqueues step i while
+    the device still runs step i - 1, then waits for step i - 1's output (double-buffered pinned inputs
+    and outputs; stream order keeps each plan's metadata copy behind the previous run)."""
     import torch
 
     import paged_kv_attention_slot_gb300 as pk
 
     kw = _plan_kw(b)
-    # the step's inputs (Q, the new K/V rows, slot_mapping) packed in one pinned host buffer and
-    # copied to one device buffer with a single H2D copy; the device tensors are views of it
+    # a step's inputs packed in one pinned host buffer and copied to one device buffer with a single
+    # H2D copy; the device tensors are views of it
     parts = [b.q.contiguous().view(torch.uint8).reshape(-1), b.k_new.contiguous().view(torch.uint8).reshape(-1),
              b.v_new.contiguous().view(torch.uint8).reshape(-1),
              torch.from_numpy(b.slot_mapping).contiguous().view(torch.uint8).reshape(-1)]
     offs = [0]
     for t in parts:
         offs.append(offs[-1] + (t.numel() + 255) // 256 * 256)
-    h_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
-    for t, o in zip(parts, offs):
-        h_in[o:o + t.numel()] = t
-    d_in = torch.empty(offs[-1], dtype=torch.uint8, device=st["q"].device)
-    q = d_in[offs[0]:offs[0] + parts[0].numel()].view(torch.bfloat16).view(b.q.shape)
-    k_new = d_in[offs[1]:offs[1] + parts[1].numel()].view(torch.bfloat16).view(b.k_new.shape)
-    v_new = d_in[offs[2]:offs[2] + parts[2].numel()].view(torch.bfloat16).view(b.v_new.shape)
-    slots = d_in[offs[3]:offs[3] + parts[3].numel()].view(torch.int64)
-    hout = torch.empty_like(b.q).pin_memory()
+    bufs = []
+    for _ in range(2):
+        h_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+        for t, o in zip(parts, offs):
+            h_in[o:o + t.numel()] = t
+        d_in = torch.empty(offs[-1], dtype=torch.uint8, device=st["q"].device)
+        views = (d_in[offs[0]:offs[0] + parts[0].numel()].view(torch.bfloat16).view(b.q.shape),
+                 d_in[offs[1]:offs[1] + parts[1].numel()].view(torch.bfloat16).view(b.k_new.shape),
+                 d_in[offs[2]:offs[2] + parts[2].numel()].view(torch.bfloat16).view(b.v_new.shape),
+                 d_in[offs[3]:offs[3] + parts[3].numel()].view(torch.int64))
+        bufs.append((h_in, d_in, views, torch.empty_like(b.q).pin_memory(), torch.cuda.Event()))
     stream = torch.cuda.current_stream()
 
-    def step():
+    def enqueue(i):
+        h_in, d_in, (q, k_new, v_new, slots), hout, done = bufs[i & 1]
         d_in.copy_(h_in, non_blocking=True)
         # the KV write needs no plan: the GPU stores this step's rows while the host plans
         pk.kv_store(k_new, v_new, slots, st["cache"], stream=stream)
         plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, stream=stream, **kw)
         plan.run(q, st["cache"], out=st["out"], stream=stream)
         hout.copy_(st["out"], non_blocking=True)
-        stream.synchronize()
+        done.record(stream)
 
-    for _ in range(warmup):
-        step()
+    def run(n):
+        for i in range(n):
+            enqueue(i)
+            if i > 0:
+                bufs[(i - 1) & 1][4].synchronize()  # step i - 1's output is on the host
+        bufs[(n - 1) & 1][4].synchronize()
+
+    run(warmup)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
+    run(steps)
     dt = time.perf_counter() - t0
     h2d = sum(t.numel() for t in parts)  # bytes of Q, K/V rows and slots (padding excluded)
     h2d += sum(a.nbytes for a in (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len))
-    d2h = hout.numel() * hout.element_size()
+    d2h = bufs[0][3].numel() * bufs[0][3].element_size()
     return dt, h2d, d2h
 
 
