@@ -528,6 +528,73 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    if (rows * D <= 4 * 128) {
+      // One float4 column per thread (up to 4 rows of 128 dims): an online merge.  Each thread loads
+      // the log2-sum-exp of its row and its column of U partials at once (as many as its registers
+      // hold: 20 with 4 resident CTAs, 32 with 2) and folds them in under a running maximum, so 38
+      // partials cost two dependent L2 round trips and no shared-memory staging.
+      constexpr int U = C::CTAS >= 4 ? 20 : 32;
+      const int ns = mi_.num_splits;
+      const int n4 = rows * D / 4;
+      const int col = threadIdx.x;
+      const bool active = col < n4;
+      const int crow = active ? col * 4 / D : 0;
+      const float* lse_g = p.part_lse + (int64_t)mi_.first_slot * kDecodeRows + crow;
+      const float4* pm = reinterpret_cast<const float4*>(p.part_o + (int64_t)mi_.first_slot * kDecodeRows * D) + col;
+      constexpr int SLOT4 = kDecodeRows * D / 4;
+      float la[U];
+      float4 oa[U];
+      auto fetch = [&](float (&l)[U], float4 (&o)[U], int s0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const bool in = active && s0 + u < ns;
+          l[u] = in ? __ldcg(lse_g + (int64_t)(s0 + u) * kDecodeRows) : -INFINITY;
+          o[u] = in ? __ldcg(pm + (int64_t)(s0 + u) * SLOT4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      };
+      float m = -INFINITY, W = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      auto fold = [&](const float (&l)[U], const float4 (&o)[U]) {
+        float mb = m;
+#pragma unroll
+        for (int u = 0; u < U; ++u) mb = fmaxf(mb, l[u]);
+        if (mb == -INFINITY) return;  // a partial without keys has lse -inf and weight 0
+        const float c = ex2(m - mb);  // 0 while nothing has been seen
+        W *= c;
+        acc.x *= c;
+        acc.y *= c;
+        acc.z *= c;
+        acc.w *= c;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float wv = ex2(l[u] - mb);
+          W += wv;
+          acc.x = fmaf(wv, o[u].x, acc.x);
+          acc.y = fmaf(wv, o[u].y, acc.y);
+          acc.z = fmaf(wv, o[u].z, acc.z);
+          acc.w = fmaf(wv, o[u].w, acc.w);
+        }
+        m = mb;
+      };
+      for (int s0 = 0; s0 < ns; s0 += U) {
+        fetch(la, oa, s0);
+        fold(la, oa);
+      }
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o) + ((int64_t)mi_.q_row * p.num_qo_heads + qh0) * D;
+      if (active) {
+        const float f = W > 0.f ? p.out_scale / W : 0.f;
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + col * 4);
+        o2[0] = __floats2bfloat162_rn(acc.x * f, acc.y * f);
+        o2[1] = __floats2bfloat162_rn(acc.z * f, acc.w * f);
+        if (p.lse && (col * 4) % D == 0)  // the row's first column writes its log-sum-exp
+          p.lse[(int64_t)mi_.q_row * p.num_qo_heads + qh0 + crow] = (m + __log2f(W)) * 0.69314718055994531f;
+      }
+      if (threadIdx.x == 0) {  // ready for the next run of this plan
+        p.unit_count[unit] = 0;
+        atomicExch(p.claim + unit * kClaimStride, 0);
+      }
+      return;
+    }
     // Online merge over chunks of splits: the chunk's log2-sum-exps are staged in shared memory by
     // all threads and turned into per-row weights 2^(lse_s - M) once, one warp per row (lanes over
     // the splits, shuffle reductions); each thread owns float4 columns of the output and keeps 8-16
