@@ -128,16 +128,14 @@ __device__ __forceinline__ void add_scaled_bf16x8(const uint4& v, float w, float
 // One warp's share of a K or V tile: NW warps share the tile's 64 row pairs, this one (pw) copies
 // pairs pw, pw + NW, ...; in each cp.async lanes 0-15 copy the 16 chunks of the pair's first row and
 // lanes 16-31 those of its second, into the 128-byte-swizzled K-major layout (64-column halves).
-// Lane l holds the global addresses of the warp's rows l (ra) and 32 + l (rb); bit r of va / vb says
-// whether row r / 32 + r exists (else 16 zero bytes are written).  Fully unrolled: the destination of
-// pair i is a per-lane base plus a constant, because the swizzle of row 2 (pw + NW i) + hi repeats with
-// period 4 in i.
+// Lane l holds the global addresses of the warp's rows l (ra) and 32 + l (rb).  Fully unrolled: the
+// destination of pair i is a per-lane base plus a constant, because the swizzle of row 2 (pw + NW i) +
+// hi repeats with period 4 in i.
 template <int NW>
-__device__ __forceinline__ void issue_rows(uint32_t dst0, int pw, int pairs, uint64_t ra, uint64_t rb, uint32_t va,
-                                           uint32_t vb, int c, int hi) {
+__device__ __forceinline__ void issue_rows(uint32_t dst0, int pw, int pairs, uint64_t ra, uint64_t rb, int c,
+                                           int hi) {
   constexpr int MAXP = (pf::KT / 2 + NW - 1) / NW;
   const int cc = c & 7;
-  const uint32_t va_l = va >> hi, vb_l = vb >> hi;
   uint32_t base[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -148,9 +146,8 @@ __device__ __forceinline__ void issue_rows(uint32_t dst0, int pw, int pairs, uin
   for (int i = 0; i < MAXP; ++i) {
     if (i == MAXP - 1 && i >= pairs) break;  // only the last pair can be missing (V warps)
     const uint64_t src = __shfl_sync(0xffffffffu, i < 16 ? ra : rb, (2 * i + hi) & 31);
-    const bool valid = ((i < 16 ? va_l : vb_l) >> ((2 * i) & 31)) & 1u;
     const uint32_t dst = base[i & 3] + (uint32_t)((i >> 2) * 8 * NW * 128);
-    cp_async16(dst, reinterpret_cast<const char*>(src) + c * 16, valid ? 16u : 0u);
+    cp_async16(dst, reinterpret_cast<const char*>(src) + c * 16, 16u);
   }
 }
 
@@ -281,23 +278,21 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       return pool + slot * p.stride_token_b + head_off;
     };
     // Lane l resolves the addresses of this warp's rows l and 32 + l of a tile one tile ahead (the
-    // page-table loads overlap the wait for the stage); a missing row reads from `pool` with a zero
-    // source size.  The validity bits of all lanes' rows travel as two ballots.
+    // page-table loads overlap the wait for the stage).  A row past the item's last key copies the
+    // row of its first key instead of zeros: its score is masked to -inf and its probability is 0,
+    // and a real row's values are finite, so it adds nothing (the split chunks of an item are whole
+    // tiles, so only the item's end, where the mask applies, has such rows).
     const int nrows = 2 * pairs;
+    const char* first_row = row_addr(w.kv_begin);
+    if (!first_row) first_row = pool;  // a page outside the pool (recorded): any readable row
     struct Rows {
       uint64_t a, b;
-      uint32_t va, vb;
     };
     auto resolve = [&](int tile) -> Rows {
       const int k0 = w.kv_begin + tile * KT;
       const char* ra = lane < nrows ? row_addr(k0 + row_of(lane)) : nullptr;
       const char* rb = 32 + lane < nrows ? row_addr(k0 + row_of(32 + lane)) : nullptr;
-      Rows r;
-      r.va = __ballot_sync(0xffffffffu, ra != nullptr);
-      r.vb = __ballot_sync(0xffffffffu, rb != nullptr);
-      r.a = (uint64_t)(ra ? ra : pool);
-      r.b = (uint64_t)(rb ? rb : pool);
-      return r;
+      return Rows{(uint64_t)(ra ? ra : first_row), (uint64_t)(rb ? rb : first_row)};
     };
     const int c = lane & 15, hi = lane >> 4;  // 16-byte chunk of the 256-byte row; first or second row of a pair
     bool ok = true;
@@ -310,9 +305,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       if (!ok) break;
       const uint32_t dst0 = s_base + st * TILE_B + (c >> 3) * HALF_B;
       if (is_k)
-        issue_rows<K_WARPS>(dst0, pw, pairs, cur.a, cur.b, cur.va, cur.vb, c, hi);
+        issue_rows<K_WARPS>(dst0, pw, pairs, cur.a, cur.b, c, hi);
       else
-        issue_rows<V_WARPS>(dst0, pw, pairs, cur.a, cur.b, cur.va, cur.vb, c, hi);
+        issue_rows<V_WARPS>(dst0, pw, pairs, cur.a, cur.b, c, hi);
       // the stage's barrier receives this thread's arrival when its copies have landed; the MMA
       // thread fences them into the async proxy after its wait
       cp_async_arrive_noinc(full0 + 8 * st);
