@@ -11,8 +11,8 @@
 // GB300 design.  One CTA = two 128-row query tiles (A and B: consecutive tokens of one request, rows
 // = (token, head) pairs of one KV head's query-head group) sharing every K/V tile, so each gathered
 // K/V byte feeds twice the tensor-core work of a single tile:
-//  * warps 8-11 and 13-15 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle); K (warps
-//    8-11) and V (warps 13-15) tiles of 128 keys gathered row by row through the page table with
+//  * warps 8-11 and 13-15 (producers): Q_A and Q_B by 3-D TMA boxes (128-byte swizzle, warp 8); K
+//    (warps 9-11) and V (warps 13-15) tiles of 128 keys gathered row by row through the page table with
 //    16-byte cp.async, 16 lanes per 256-byte row, straight into the 128-byte-swizzled layout the
 //    tensor core reads; two stages.  Each lane resolves the global addresses of two of its warp's
 //    rows of the next tile while the stage is still in use, so the unrolled copy loop spends one
@@ -82,12 +82,12 @@ enum {
 constexpr uint32_t TMEM_COLS = 512;  // S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384), O_B [384,512)
 constexpr uint32_t TMEM_O = 256;
 constexpr int THREADS = 512;          // 4 warpgroups: softmax A, softmax B, producers, MMA + producers
-constexpr int PRODUCER_WARP0 = 8;     // warps 8-11 and 13-15 gather K and V
+constexpr int PRODUCER_WARP0 = 8;     // warp 8 loads Q; warps 9-11 and 13-15 gather K and V
 constexpr int MMA_WARP = 12;
-// Producer roles: K by warps 8-11 and V by warps 13-15 (K is needed first, by S).  Warp w runs on
-// scheduler w % 4, so each of schedulers 1-3 carries one K and one V warp (16 + 21-22 row pairs a
-// tile) and scheduler 0, which also runs the MMA thread, one K warp.
-constexpr int K_WARPS = 4, V_WARPS = 3;
+// Producer roles: K by warps 9-11 and V by warps 13-15 (K is needed first, by S); warp 8 only loads
+// Q.  Warp w runs on scheduler w % 4, so each of schedulers 1-3 carries one K and one V warp (21-22
+// row pairs of each a tile) and scheduler 0 is left to the MMA thread, whose issue rate it sets.
+constexpr int K_WARPS = 3, V_WARPS = 3;
 // launched at 65536 / 512 = 128 registers per thread, then rebalanced per warpgroup:
 // 2 x 128 x SOFTMAX_REGS + 2 x 128 x OTHER_REGS = 47104 + 18432 = 65536 <= 65536
 constexpr uint32_t SOFTMAX_REGS = 184;
@@ -228,8 +228,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     tc::reg_dealloc<OTHER_REGS>();
     // role: operand and index among that operand's warps; warp k of n copies the row pairs
     // q = k, k + n, k + 2n, ... (rows 2q and 2q + 1, 16 lanes per 256-byte row)
-    const bool is_k = warp < MMA_WARP;  // K: warps 8-11, V: warps 13-15
-    const int pw = is_k ? warp - PRODUCER_WARP0 : warp - MMA_WARP - 1;
+    const bool is_k = warp < MMA_WARP;  // K: warps 9-11, V: warps 13-15 (warp 8 loads Q only)
+    const int pw = is_k ? warp - PRODUCER_WARP0 - 1 : warp - MMA_WARP - 1;
     const int nw = is_k ? K_WARPS : V_WARPS;
     const int pairs = (KT / 2 - pw + nw - 1) / nw;  // row pairs of this warp per tile
     auto row_of = [&](int idx) -> int { return 2 * (pw + nw * (idx >> 1)) + (idx & 1); };  // idx-th row
@@ -282,8 +282,9 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     // row of its first key instead of zeros: its score is masked to -inf and its probability is 0,
     // and a real row's values are finite, so it adds nothing (the split chunks of an item are whole
     // tiles, so only the item's end, where the mask applies, has such rows).
+    const bool gathers = warp != PRODUCER_WARP0;
     const int nrows = 2 * pairs;
-    const char* first_row = row_addr(w.kv_begin);
+    const char* first_row = gathers ? row_addr(w.kv_begin) : nullptr;
     if (!first_row) first_row = pool;  // a page outside the pool (recorded): any readable row
     struct Rows {
       uint64_t a, b;
@@ -296,8 +297,8 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     };
     const int c = lane & 15, hi = lane >> 4;  // 16-byte chunk of the 256-byte row; first or second row of a pair
     bool ok = true;
-    Rows next = resolve(0);
-    for (int j = 0; j < nkt && ok; ++j) {
+    Rows next = gathers ? resolve(0) : Rows{0, 0};
+    for (int j = 0; j < nkt && ok && gathers; ++j) {
       const int st = j & 1;
       const Rows cur = next;
       if (j + 1 < nkt) next = resolve(j + 1);
