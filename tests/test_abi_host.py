@@ -706,3 +706,17 @@ def test_cascade_run_argument_checks(pk):
     assert "lse is required" in L.pkv_last_error().decode()
     assert run(shared, suffix) == pk._lib.PKV_EINVAL  # host-only plans cannot run
     assert "host-only" in L.pkv_last_error().decode()
+
+
+def test_wait_limit_and_hold_settings(pk):
+    # the bound on the prefill kernel's waits: <= 0 restores the default, beyond 2^41 clocks is
+    # rejected; the hold switch only toggles (its effect is exercised on the GPU)
+    L = pk._lib.lib()
+    assert L.pkv_set_wait_limit(20000) == pk._lib.PKV_OK
+    assert L.pkv_set_wait_limit(0) == pk._lib.PKV_OK
+    assert L.pkv_set_wait_limit(-5) == pk._lib.PKV_OK
+    assert L.pkv_set_wait_limit(1 << 42) == pk._lib.PKV_EINVAL
+    assert "too large" in L.pkv_last_error().decode()
+    assert L.pkv_test_hold_wait(1) == pk._lib.PKV_OK
+    assert L.pkv_test_hold_wait(0) == pk._lib.PKV_OK
+    pk.set_wait_limit(0)
