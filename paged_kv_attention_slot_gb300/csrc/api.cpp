@@ -55,6 +55,7 @@ constexpr int kPrefillTiles = 2;         // Q tiles per CTA (they share every K/
 constexpr int kPrefillKeyTile = 128;     // keys per K/V tile of the prefill kernel
 constexpr int kPrefillMinChunk = 256;    // never split a prefill key range below this many keys
 constexpr int kPrefillMaxSplits = 64;    // chunks per prefill item at most (the chunk grows instead)
+constexpr bool kDecodeSplitMajor = true;   // the CTAs of a split unit spread over the launch order
 constexpr bool kPrefillGroupOrder = true;  // prefill CTAs grouped by (request, KV head) for L2 reuse
 constexpr int kPrefillTailNum = 10, kPrefillTailDen = 100;  // share of the work ordered longest first at the end
 
@@ -129,6 +130,31 @@ void order_longest_first(std::vector<WorkItem>& all, size_t begin, size_t end) {
   WorkItem* dst = tmp.data();
   for (size_t i = 0; i < n; ++i) dst[c[nb - 1 - (k[i] >> shift)]++] = w[i];
   std::memcpy(w, dst, n * sizeof(WorkItem));
+}
+
+// Split-major order of the decode items, applied before the longest-first order (which is stable):
+// split 0 of every unit, then split 1 of every unit, and so on, so the CTAs of one split unit are
+// spread over the whole launch order instead of sitting next to each other.  The block scheduler
+// fills the SMs' resident slots in launch order, and measured per-CTA timelines show the CTAs
+// launched into an SM's last slots streaming more slowly than its first ones; a unit launched as
+// one contiguous block lands on the same slot of every SM and, with the run-time claims balancing
+// only within a unit, units launched late finished ~3.5 us after units launched early.  Spread
+// over all slots, every unit streams at the same aggregate rate and all of them end together.
+void order_split_major(std::vector<WorkItem>& all, size_t begin, size_t end) {
+  const size_t n = end - begin;
+  if (n < 2) return;
+  WorkItem* w = all.data() + begin;
+  int32_t max_split = 0;
+  for (size_t i = 0; i < n; ++i) max_split = std::max(max_split, w[i].split);
+  if (max_split == 0) return;
+  thread_local std::vector<uint32_t> count;
+  thread_local std::vector<WorkItem> tmp;
+  count.assign((size_t)max_split + 2, 0u);
+  tmp.resize(n);
+  for (size_t i = 0; i < n; ++i) ++count[(size_t)w[i].split + 1];
+  for (int32_t s = 0; s <= max_split; ++s) count[(size_t)s + 1] += count[(size_t)s];
+  for (size_t i = 0; i < n; ++i) tmp[count[(size_t)w[i].split]++] = w[i];
+  std::memcpy(w, tmp.data(), n * sizeof(WorkItem));
 }
 
 // Group-major order of the prefill items on top of the longest-first order: the (request, KV head)
@@ -515,6 +541,7 @@ int build_plan(const pkv_plan_args* a, pkv_plan* P) {
     }
   }
   // longest first: the block scheduler hands out CTAs roughly in launch order
+  if (kDecodeSplitMajor) order_split_major(P->work, 0, (size_t)P->num_decode_work);
   order_longest_first(P->work, 0, (size_t)P->num_decode_work);
   order_longest_first(P->work, (size_t)P->num_decode_work, P->work.size());
   if (kPrefillGroupOrder) order_by_group(P->work, (size_t)P->num_decode_work, P->work.size(), a->num_kv_heads);

@@ -42,6 +42,21 @@ namespace pkv {
 
 int32_t* device_error_ptr();
 
+// The K/V rows are read once per launch: they are copied with an evict-first L2 policy, so the
+// stream (hundreds of MB through a 129 MB L2) does not push out the lines that are read again -- the
+// work list, the page table, the split partials and whatever the surrounding layers keep there.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+// cp.async of 16 bytes (src_bytes < 16 zero-fills the rest) under an L2 cache policy.
+__device__ __forceinline__ void cp_async16_pol(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(pol)
+               : "memory");
+}
+
 template <int D, bool FP8, int NB>
 struct DecodeCfg {
   static constexpr int ROWB = FP8 ? D : 2 * D;  // bytes per key row of one head
@@ -155,6 +170,7 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
   const uint32_t wsm_u = smem_u32(wsm);
   const int lr = lane & 15;  // row whose page this lane resolves
   const int64_t head_off = (int64_t)w.kv_head * p.stride_head_b;
+  const uint64_t kv_policy = l2_evict_first();
 
   // Lane lr (0..15) resolves the page of row lr of a tile; then every warp-wide cp.async covers
   // 32 / CH whole rows with consecutive lanes on consecutive 16-byte chunks (fully coalesced).
@@ -220,8 +236,8 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
       for (int j = 0; j < C::KEYS / RPI; ++j) {
         const int row = j * RPI + lsub;
         const uint32_t sw = row * C::ROWB + ((lc ^ (row & 7)) << 4);
-        cp_async16(dk + sw, ks + j * row_step, 16u);
-        cp_async16(dv + sw, vs + j * row_step, 16u);
+        cp_async16_pol(dk + sw, ks + j * row_step, 16u, kv_policy);
+        cp_async16_pol(dv + sw, vs + j * row_step, 16u, kv_policy);
       }
       return;
     }
@@ -239,8 +255,8 @@ __global__ void __launch_bounds__(128, DecodeCfg<D, FP8, NB>::CTAS) decode_kerne
       const int64_t o = __shfl_sync(0xffffffffu, roff, row);
       const uint32_t sw = row * C::ROWB + ((lc ^ (row & 7)) << 4);
       const bool ok = o >= 0;
-      cp_async16(dk + sw, ok ? p.k_pool + o + lc * 16 : p.k_pool, ok ? 16u : 0u);
-      cp_async16(dv + sw, ok ? p.v_pool + o + lc * 16 : p.v_pool, ok ? 16u : 0u);
+      cp_async16_pol(dk + sw, ok ? p.k_pool + o + lc * 16 : p.k_pool, ok ? 16u : 0u, kv_policy);
+      cp_async16_pol(dv + sw, ok ? p.v_pool + o + lc * 16 : p.v_pool, ok ? 16u : 0u, kv_policy);
     }
   };
 

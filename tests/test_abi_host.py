@@ -187,6 +187,30 @@ def test_decode_partition_covers_every_key_once(pk, n):
     assert info["kv_tokens"] == int(b.kv_len.sum())
 
 
+def test_decode_split_units_spread_over_the_launch_order(pk):
+    # two 131,072-key FP8 requests x 8 KV heads: 16 split units of 38 CTAs each.  Equal shares are
+    # launched split-major (split 0 of every unit, then split 1, ...), so every unit has CTAs in each
+    # quarter of the launch order (the SMs' resident slots fill in launch order).
+    import workloads as W
+
+    b = W.workload(5)
+    p = pk.Plan().plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, num_qo_heads=b.num_qo_heads,
+                       num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, page_size=b.page_size, mode="decode",
+                       kv_dtype="e4m3", num_sms=152, host_only=True)
+    items = p.work_items()
+    n = len(items)
+    unit = items[:, 0] * b.num_kv_heads + items[:, 1]
+    units = np.unique(unit)
+    assert len(units) == 16 and n == 16 * (n // 16) and n // 16 > 8
+    for u in units:
+        pos = np.nonzero(unit == u)[0]
+        quarters = np.bincount(pos * 4 // n, minlength=4)
+        assert quarters.min() >= len(pos) // 4 - 1
+    # round robin over the units: each run of 16 consecutive CTAs holds one CTA of every unit
+    assert all(len(set(unit[i:i + 16].tolist())) == 16 for i in range(0, n, 16))
+    _check_decode_cover(b, items, group=b.num_qo_heads // b.num_kv_heads)
+
+
 def test_decode_order_with_more_ctas_than_buckets(pk):
     # 1,200 requests x 8 KV heads = 9,600 CTAs: the counting sort's bucket count is clamped at 4096
     rng = np.random.default_rng(17)
