@@ -465,9 +465,14 @@ def kernel_ms(run_once, reps=20, iters=7):
 def run_e2e(b, st, plan, steps, warmup):
     """Same step through the public API from pinned HOST buffers: every step copies its inputs (Q,
     the new K/V rows, slot_mapping) host -> device, re-plans, writes the KV, runs, and copies O back
-    to the host.  Steps are pipelined as a serving loop would: the host plans and enqueues step i while
-    the device still runs step i - 1, then waits for step i - 1's output (double-buffered pinned inputs
-    and outputs; stream order keeps each plan's metadata copy behind the previous run)."""
+    to the host.  Steps are pipelined as a serving loop would run them: the copies go on two copy
+    streams (H2D and D2H) so that step i's input copy overlaps step i - 1's kernels and step i's
+    output copy overlaps step i + 1's; the host plans and enqueues step i while the device still runs
+    step i - 1, then waits for step i - 1's output.  Pinned inputs, device inputs, device outputs and
+    pinned outputs are double-buffered, and events order every reuse of a buffer (stream order keeps
+    each plan's metadata copy behind the previous run).  Returns the wall time, the H2D and D2H bytes
+    per step, and the largest difference between the last step's output on the host and the same
+    step timed on the device."""
     import torch
 
     import paged_kv_attention_slot_gb300 as pk
@@ -481,45 +486,64 @@ def run_e2e(b, st, plan, steps, warmup):
     offs = [0]
     for t in parts:
         offs.append(offs[-1] + (t.numel() + 255) // 256 * 256)
+    dev = st["q"].device
     bufs = []
     for _ in range(2):
         h_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
         for t, o in zip(parts, offs):
             h_in[o:o + t.numel()] = t
-        d_in = torch.empty(offs[-1], dtype=torch.uint8, device=st["q"].device)
+        d_in = torch.empty(offs[-1], dtype=torch.uint8, device=dev)
         views = (d_in[offs[0]:offs[0] + parts[0].numel()].view(torch.bfloat16).view(b.q.shape),
                  d_in[offs[1]:offs[1] + parts[1].numel()].view(torch.bfloat16).view(b.k_new.shape),
                  d_in[offs[2]:offs[2] + parts[2].numel()].view(torch.bfloat16).view(b.v_new.shape),
                  d_in[offs[3]:offs[3] + parts[3].numel()].view(torch.int64))
-        bufs.append((h_in, d_in, views, torch.empty_like(b.q).pin_memory(), torch.cuda.Event()))
-    stream = torch.cuda.current_stream()
+        bufs.append({"h_in": h_in, "d_in": d_in, "views": views, "d_out": torch.empty_like(st["out"]),
+                     "h_out": torch.empty_like(b.q).pin_memory(), "in_ready": torch.cuda.Event(),
+                     "run_done": torch.cuda.Event(), "out_copied": torch.cuda.Event()})
+    compute = torch.cuda.current_stream()
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
 
     def enqueue(i):
-        h_in, d_in, (q, k_new, v_new, slots), hout, done = bufs[i & 1]
-        d_in.copy_(h_in, non_blocking=True)
+        B = bufs[i & 1]
+        q, k_new, v_new, slots = B["views"]
+        if i >= 2:  # step i - 2's kernels have read this input buffer
+            h2d_stream.wait_event(B["run_done"])
+        with torch.cuda.stream(h2d_stream):
+            B["d_in"].copy_(B["h_in"], non_blocking=True)
+        B["in_ready"].record(h2d_stream)
+        compute.wait_event(B["in_ready"])
         # the KV write needs no plan: the GPU stores this step's rows while the host plans
-        pk.kv_store(k_new, v_new, slots, st["cache"], stream=stream)
-        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, stream=stream, **kw)
-        plan.run(q, st["cache"], out=st["out"], stream=stream)
-        hout.copy_(st["out"], non_blocking=True)
-        done.record(stream)
+        pk.kv_store(k_new, v_new, slots, st["cache"], stream=compute)
+        plan.plan(b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len, stream=compute, **kw)
+        if i >= 2:  # step i - 2's output has left this device buffer
+            compute.wait_event(B["out_copied"])
+        plan.run(q, st["cache"], out=B["d_out"], stream=compute)
+        B["run_done"].record(compute)
+        d2h_stream.wait_event(B["run_done"])
+        with torch.cuda.stream(d2h_stream):
+            B["h_out"].copy_(B["d_out"], non_blocking=True)
+        B["out_copied"].record(d2h_stream)
 
     def run(n):
         for i in range(n):
             enqueue(i)
             if i > 0:
-                bufs[(i - 1) & 1][4].synchronize()  # step i - 1's output is on the host
-        bufs[(n - 1) & 1][4].synchronize()
+                bufs[(i - 1) & 1]["out_copied"].synchronize()  # step i - 1's output is on the host
+        bufs[(n - 1) & 1]["out_copied"].synchronize()
 
     run(warmup)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     run(steps)
     dt = time.perf_counter() - t0
+    torch.cuda.synchronize()
     h2d = sum(t.numel() for t in parts)  # bytes of Q, K/V rows and slots (padding excluded)
     h2d += sum(a.nbytes for a in (b.qo_indptr, b.kv_indptr, b.kv_indices, b.last_page_len))
-    d2h = bufs[0][3].numel() * bufs[0][3].element_size()
-    return dt, h2d, d2h
+    d2h = bufs[0]["h_out"].numel() * bufs[0]["h_out"].element_size()
+    # the host copy of the last step against the device-timed path's output on the same inputs
+    diff = float((bufs[(steps - 1) & 1]["h_out"].float() - st["out"].cpu().float()).abs().max())
+    return dt, h2d, d2h, diff
 
 
 def decode_other_configs(device, hbm):
@@ -795,8 +819,9 @@ def main():
     kv_bytes = b.kv_bytes_read()
     value = aggregate_gbs(kv_bytes, args.steps, world, max_ms)
 
-    e2e_dt, h2d, d2h = run_e2e(b, st, plan, max(3, args.steps // 2), 3)
-    e2e_val = kv_bytes * max(3, args.steps // 2) / e2e_dt / 1e9
+    e2e_steps = max(20, args.steps)
+    e2e_dt, h2d, d2h, e2e_diff = run_e2e(b, st, plan, e2e_steps, 3)
+    e2e_val = kv_bytes * e2e_steps / e2e_dt / 1e9
     err = pk.device_error()
 
     _, run_ms = run_steps(b, st, plan, min(args.steps, 10), 1, False, record_run_events=True)  # diagnostic
@@ -854,7 +879,8 @@ def main():
                          "kernel_ms": round(k_ms, 4), "timing": k_mode,
                          "run_ms_mean_in_steps": round(run_avg, 4),
                          "traffic": _traffic("decode", DECODE_SOURCES)},
-            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps, "max_abs_vs_device_path": round(e2e_diff, 5)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
