@@ -870,9 +870,18 @@ int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* 
   // the slot rows the kernel computes are 32-bit
   if (cache->num_pages * (int64_t)cache->page_size > INT32_MAX)
     return fail(PKV_EUNSUPPORTED, "prefill needs num_pages * page_size < 2^31");
-  // K/V are gathered with cp.async through the page table: the kernel's K/V tensor-map parameters
-  // are not read, and are passed zeroed
-  alignas(64) CUtensorMap tk{}, tv{};
+  // O: the same 3-D view and box as Q (full output tiles go out by TMA stores of the box they came in)
+  alignas(64) CUtensorMap to;
+  {
+    const int G = plan->Hq / plan->Hkv;
+    cuuint64_t dims[3] = {(cuuint64_t)plan->D, (cuuint64_t)plan->Hq, (cuuint64_t)plan->total_tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)plan->D * 2, (cuuint64_t)plan->Hq * plan->D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(128 / G)};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = encode(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled(O) failed: " + std::to_string((int)r));
+  }
   pkv::RunParams p = make_params(plan, q, cache, o, lse, first, count);
   p.merge_into = merge ? 1 : 0;
   if (plan->paged_ragged) {
@@ -880,7 +889,7 @@ int run_prefill(const pkv_plan* plan, int mode, const void* q, const pkv_cache* 
     p.ext_v = static_cast<const char*>(v_new);
     p.ext_row_b = (int64_t)plan->Hkv * plan->D * 2;
   }
-  PKV_CUDA(pkv::launch_prefill(p, &tq, &tk, &tv, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
+  PKV_CUDA(pkv::launch_prefill(p, &tq, &to, plan->total_tokens, (cudaStream_t)stream), "prefill launch");
   const int64_t nm = (int64_t)plan->merge.size() - plan->num_decode_merge;
   if (nm > 0)
     PKV_CUDA(pkv::launch_prefill_merge(p, plan->num_decode_merge, nm, (cudaStream_t)stream), "prefill merge launch");

@@ -109,8 +109,8 @@ cudaError_t launch_kv_store(const void* k, const void* v, const int64_t* slots, 
                             float inv_k, float inv_v, cudaStream_t s);
 cudaError_t launch_decode(const RunParams& p, int kv_dtype, cudaStream_t s);
 int decode_ctas_per_sm(int kv_dtype, int head_dim, int group);  // resident decode CTAs per SM
-cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v,
-                           int64_t total_tokens, cudaStream_t s);
+cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_o, int64_t total_tokens,
+                           cudaStream_t s);
 int prefill_supported(const char** why);
 cudaError_t launch_prefill_merge(const RunParams& p, int64_t first_merge, int64_t count, cudaStream_t s);
 // copy of plan metadata from a mapped pinned host buffer (device alias src_mapped) to the workspace

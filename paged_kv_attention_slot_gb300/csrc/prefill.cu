@@ -36,7 +36,8 @@
 //    window masking only on tiles that need it.  The row maximum moves lazily (only when it grows
 //    by more than 2^8; exact because numerator and denominator share it), and O is rescaled in TMEM
 //    only then, before the first half is signalled.  Epilogue: O / l to bf16 rows and the LSE, or an
-//    fp32 partial of a split item.
+//    fp32 partial of a split item; a tile whose rows all belong to the item is staged in its Q
+//    buffer in the swizzled layout of the Q box and leaves by two TMA stores.
 // Registers are rebalanced with setmaxnreg: the two softmax warpgroups take 184 per thread, the
 // producer and MMA warpgroups keep 72.  Every wait is bounded: on timeout the CTA records PKV_DEVERR_TIMEOUT, waits (bounded) for its own
 // copies and MMAs, frees its TMEM and exits.
@@ -65,7 +66,7 @@ constexpr int OFF_QB = OFF_QA + TILE_B;
 constexpr int OFF_K = OFF_QB + TILE_B;
 constexpr int OFF_V = OFF_K + STAGES * TILE_B;
 constexpr int OFF_BAR = OFF_V + STAGES * TILE_B;
-constexpr int NUM_BARS = 19;
+constexpr int NUM_BARS = 21;
 constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_TMEM + 8;
 constexpr int SMEM_USED = OFF_ABORT + 8;
@@ -77,7 +78,8 @@ enum {
   B_OD = 13,  // [2]: the last PV_X complete
   B_FIN = 15,
   B_PH = 16,  // [2]: the first half (keys 0-63) of P_X(j) stored by the 4 softmax warps of tile X
-  B_HOLD = 18  // nothing arrives here: the held wait of a timeout-path test
+  B_HOLD = 18,  // nothing arrives here: the held wait of a timeout-path test
+  B_OS = 19     // [2]: tile X's output rows staged in its Q buffer by its 4 softmax warps
 };
 constexpr uint32_t TMEM_COLS = 512;  // S_A/P_A [0,128), S_B/P_B [128,256), O_A [256,384), O_B [384,512)
 constexpr uint32_t TMEM_O = 256;
@@ -152,8 +154,8 @@ __device__ __forceinline__ void issue_rows(uint32_t dst0, int pw, int pairs, uin
 }
 
 __global__ void __launch_bounds__(pf::THREADS, 1)
-    prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                   const __grid_constant__ CUtensorMap tv, int32_t* err) {
+    prefill_kernel(const RunParams p, const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap to,
+                   int32_t* err) {
   using namespace pf;
   pdl_wait();  // the plan's metadata copy and the KV write before this run must be complete
   extern __shared__ uint8_t smem_raw[];
@@ -174,8 +176,6 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
   const bool two = w.q_rows > T;       // does tile B hold any token?
   const int nkt = (w.kv_end - w.kv_begin + KT - 1) / KT;
   const long long wait_limit = (long long)p.wait_limit_k << 10;
-  (void)tk;
-  (void)tv;
 
   if (nkt == 0) {
     // a non-causal segment without keys: the empty state (o = 0, lse = -inf) for every row.
@@ -209,6 +209,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       tc::mbar_init(BAR(B_PF + x), 4);
       tc::mbar_init(BAR(B_PH + x), 4);
       tc::mbar_init(BAR(B_OD + x), 1);
+      tc::mbar_init(BAR(B_OS + x), 4);
     }
     tc::mbar_init(BAR(B_FIN), 1);
     tc::mbar_init(BAR(B_HOLD), 1);
@@ -542,27 +543,66 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
       float w_prev = 0.f, w_this = 1.f;
       if (p.merge_into && row_valid) merge_weights(p.lse[row * p.num_qo_heads + head], lse_out, w_prev, w_this);
       const float inv = (l > 0.f ? 1.f / l : 0.f) * w_this;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D);
+      if (!p.merge_into && (x + 1) * T <= w.q_rows) {
+        // Every row of the tile is a token of this item: the rows go out as the Q tile came in -- into
+        // the Q tile's shared memory (free: every MMA that read it is complete), in the 128-byte
+        // swizzled layout of the same 3-D box, then one TMA store per 64-column half.  (A partial
+        // tile's box would also cover the next request's rows, so those take the per-thread stores.)
+        const uint32_t srow = sQ + (uint32_t)x * TILE_B + (uint32_t)r * 128;
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t o[32];
-        tc::tmem_ld32(tO + h * 32, o);
-        if (row_valid) {
+        for (int h = 0; h < 4; ++h) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + h * 32, o);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            float f[8];
+            uint32_t u[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv;
-            if (p.merge_into) {
-              const uint4 prev = dst[h * 4 + q];
-              add_scaled_bf16x8(prev, w_prev, f);
+            for (int e = 0; e < 4; ++e)
+              u[e] = pack_bf16(__uint_as_float(o[8 * q + 2 * e]) * inv, __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+            const int c = (h & 1) * 4 + q;  // 16-byte chunk within the 64-column half h / 2
+            tc::st_shared_v4(srow + (h >> 1) * HALF_B + ((c ^ (r & 7)) << 4), u[0], u[1], u[2], u[3]);
+          }
+        }
+        // each warp's rows into the async proxy, then one arrival per warp; thread 0 of the tile waits
+        // (bounded) for all four and stores the box
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(BAR(B_OS + x));
+        if (r == 0) {
+          if (tc::mbar_wait(BAR(B_OS + x), 0, abort_flag, wait_limit)) {
+            const int c1 = w.kv_head * G, c2 = w.q_row + x * T;
+            tc::tma_store_3d(&to, sQ + x * TILE_B, 0, c1, c2);
+            tc::tma_store_3d(&to, sQ + x * TILE_B + HALF_B, 64, c1, c2);
+            tc::bulk_commit_group();
+            tc::bulk_wait_group_read0();  // the shared memory must stay put until the stores have read it
+          } else {
+            *abort_flag = 1;
+            record_error(err, PKV_DEVERR_TIMEOUT);
+          }
+        }
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (row * p.num_qo_heads + head) * D);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          uint32_t o[32];
+          tc::tmem_ld32(tO + h * 32, o);
+          if (row_valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(o[8 * q + e]) * inv;
+              if (p.merge_into) {
+                const uint4 prev = dst[h * 4 + q];
+                add_scaled_bf16x8(prev, w_prev, f);
+              }
+              uint4 u;
+              u.x = pack_bf16(f[0], f[1]);
+              u.y = pack_bf16(f[2], f[3]);
+              u.z = pack_bf16(f[4], f[5]);
+              u.w = pack_bf16(f[6], f[7]);
+              dst[h * 4 + q] = u;
             }
-            uint4 u;
-            u.x = pack_bf16(f[0], f[1]);
-            u.y = pack_bf16(f[2], f[3]);
-            u.z = pack_bf16(f[4], f[5]);
-            u.w = pack_bf16(f[6], f[7]);
-            dst[h * 4 + q] = u;
           }
         }
       }
@@ -687,8 +727,7 @@ int prefill_supported(const char** why) {
   return 1;
 }
 
-cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_k, const void* tmap_v, int64_t,
-                           cudaStream_t s) {
+cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* tmap_o, int64_t, cudaStream_t s) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -700,8 +739,7 @@ cudaError_t launch_prefill(const RunParams& p, const void* tmap_q, const void* t
   int32_t* err = device_error_ptr();
   if (!err) return cudaErrorInvalidDevice;
   return launch_pdl(prefill_kernel, dim3((unsigned)p.num_work), dim3(pf::THREADS), (size_t)pf::SMEM_ALLOC, s, p,
-                    *static_cast<const CUtensorMap*>(tmap_q), *static_cast<const CUtensorMap*>(tmap_k),
-                    *static_cast<const CUtensorMap*>(tmap_v), err);
+                    *static_cast<const CUtensorMap*>(tmap_q), *static_cast<const CUtensorMap*>(tmap_o), err);
 }
 
 }  // namespace pkv
